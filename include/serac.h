@@ -1,0 +1,162 @@
+/*
+ * serac.h -- C ABI of libserac_gb300.so: exhaustive SIFT descriptor matching with a
+ * fused top-2 on GB300 (sm_103a).
+ *
+ * What is computed (the method of the "SERAC" page -- a fused descriptor matcher for
+ * COLMAP -- sections "What changed" and "Exactness"):
+ *
+ *   s(i, j) = sum_{k<128} a[i][k] * b[j][k]      exact integer, 0 <= s <= 8,323,200
+ *
+ *   row top-2    (s1, j1, s2, j2) of row i: the two best positive scores of the row,
+ *                ordered by score descending then column ascending, each padded with
+ *                (0, -1) ("Exactness": identity (0, -1, 0), zero floor, smallest
+ *                column on an exact top-1 tie);
+ *   column top-2 (c1, i1, c2, i2) of column j: the same over rows ("GPU kernel time":
+ *                the column direction, ColMatch, feeds the cross check);
+ *   test(t)      t.j1 >= 0  and  den * (N - t.s1) < num * (N - t.s2)  and
+ *                t.s1 >= min_score   (evaluated in 64-bit integers; the page fixes
+ *                only max_ratio <= 1, default 0.8, and that a tie rejects -- this is
+ *                the chord-distance ratio squared, r^2 = num/den, N = 512^2);
+ *   match        (i, j1(i)) is kept iff test(row i) and, when `mutual`, i1(j1(i)) == i,
+ *                and, when `col_ratio`, test(column j1(i)).  Matches are listed by
+ *                ascending i.
+ *
+ * The similarity matrix is never stored ("Fused row reduction": only the top two
+ * scores of each row and column survive); the contraction runs on the tcgen05
+ * tensor cores with f32 accumulation, exact because every partial sum is an
+ * integer below 2^24.
+ *
+ * Conventions for every entry point:
+ *   - descriptor arrays are DEVICE pointers to n x 128 uint8, row-major, contiguous,
+ *     16-byte aligned; they are read only;
+ *   - output arrays and the workspace are DEVICE memory owned by the caller;
+ *   - calls are asynchronous on `cuda_stream` (a cudaStream_t; NULL = legacy default
+ *     stream); results are valid once that stream has synchronised;
+ *   - a call returns a status below; a negative status means nothing was enqueued;
+ *   - sizes: 0 <= n <= SERAC_MAX_N per image.
+ *
+ * Errors found by the GPU (a bounded wait that ran out inside a kernel) are reported
+ * through `*count`, which then holds a negative status instead of a match count.
+ */
+#ifndef SERAC_H
+#define SERAC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SERAC_DIM 128
+#define SERAC_MAX_N (1 << 24)
+
+/* status codes */
+#define SERAC_OK 0
+#define SERAC_EINVAL (-1)        /* bad argument: null pointer, n out of range, misaligned */
+#define SERAC_ECAPACITY (-2)     /* (reported through count > capacity; never returned) */
+#define SERAC_ECUDA (-3)         /* a CUDA runtime call failed */
+#define SERAC_ETIMEOUT (-4)      /* a bounded wait inside a kernel ran out (via *count) */
+#define SERAC_EWORKSPACE (-5)    /* workspace missing or smaller than the size query */
+#define SERAC_EUNSUPPORTED (-6)  /* current device is not sm_103 or TMA encoding unavailable */
+
+/* Matching parameters, exact integers.  serac_default_params fills them from the
+ * page's knobs (max_ratio 0.8, max angle 0.7 rad -> 16/25, N = 262144, 200499). */
+typedef struct {
+  int32_t ratio_num_sq; /* r^2 = num / den (0.8 -> 16) */
+  int32_t ratio_den_sq; /*                 (0.8 -> 25) */
+  int32_t norm_sq;      /* N, squared norm of a unit descriptor at scale 512: 262144 */
+  int32_t min_score;    /* distance gate: s1 >= ceil(cos(max_angle) * N) */
+  int32_t mutual;       /* 1: require i1(j1(i)) == i */
+  int32_t col_ratio;    /* 1: column j1(i) must pass the same test */
+} serac_params;
+
+/* One image pair for match_batch (device pointers, as for match_pair). */
+typedef struct {
+  const uint8_t* a;
+  int32_t n_a;
+  const uint8_t* b;
+  int32_t n_b;
+} serac_pair;
+
+/* Outputs of one pair (device pointers, owned by the caller).
+ *   matches  [capacity][2] int32 (i, j), ascending i; at most `capacity` are written
+ *   count    1 int32: the total number of matches (may exceed capacity: then only the
+ *            first `capacity` were written) or a negative status from the GPU;
+ *            capacity n_a always suffices (min(n_a, n_b) when `mutual` is set)
+ *   row_top2 optional (NULL to skip): [n_a][4] int32 (s1, j1, s2, j2)
+ *   col_top2 optional (NULL to skip): [n_b][4] int32 (c1, i1, c2, i2) */
+typedef struct {
+  int32_t* matches;
+  int32_t capacity;
+  int32_t* count;
+  int32_t* row_top2;
+  int32_t* col_top2;
+} serac_out;
+
+/* Fill `p` from a ratio (read to 4 decimals, squared and reduced to num/den) and a
+ * maximum angle in radians (min_score = ceil(cos(angle) * 262144)); mutual = 1,
+ * col_ratio = 1.  Host only.  Returns SERAC_EINVAL if p is NULL, max_ratio is not in
+ * (0, 1] or the angle is not in [0, pi/2]. */
+int serac_default_params(serac_params* p, float max_ratio, float max_angle_rad);
+
+/* Workspace bytes match_pair needs for these sizes (host only; never fails). */
+size_t serac_pair_workspace_size(int32_t n_a, int32_t n_b);
+
+/* Match one pair (the method above).  `workspace` is device memory of at least
+ * serac_pair_workspace_size(n_a, n_b) bytes, 256-byte aligned; its contents need no
+ * initialisation and are scratch for this call (calls sharing a workspace must not
+ * overlap on the GPU).  Returns SERAC_OK once all kernels are enqueued. */
+int match_pair(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b, int32_t n_b,
+               const serac_params* params, const serac_out* out,
+               void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Workspace bytes match_batch needs for these pairs (host only).  Images that appear
+ * in several pairs (same pointer and size) are staged once. */
+size_t match_batch_workspace_size(const serac_pair* pairs, int32_t n_pairs);
+
+/* Match every pair of `pairs` (host array) into outs[k] (host array of device
+ * outputs).  Equivalent to match_pair on each pair in turn, scheduled as a few
+ * persistent launches over all pairs' tiles.  Same workspace rules as match_pair. */
+int match_batch(const serac_pair* pairs, int32_t n_pairs, const serac_params* params,
+                const serac_out* outs, void* workspace, size_t workspace_bytes,
+                void* cuda_stream);
+
+/* The full score matrix S[n_a][n_b] (int32, device, row stride n_b) computed by the
+ * same tensor-core tiles as match_pair, written out instead of reduced: a check of
+ * the contraction's exactness and of "fused == unfused".  For small n only (the
+ * output is n_a * n_b * 4 bytes).  Same workspace size as match_pair. */
+int serac_scores(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b, int32_t n_b,
+                 int32_t* scores, void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Profiling hook: when both events are non-NULL (cudaEvent_t), every following
+ * match_pair / match_batch records `ev_begin` just before its fused GEMM + top-2
+ * launch and `ev_end` just after it, on the call's stream.  NULL, NULL turns it off.
+ * Process-wide setting; not thread-safe. */
+int serac_set_profile_events(void* ev_begin, void* ev_end);
+
+/* SERAC_OK if the current CUDA device is an sm_103 part this library was built for,
+ * else SERAC_EUNSUPPORTED (or SERAC_ECUDA if no device can be queried). */
+int serac_device_check(void);
+
+/* Number of kernel launches the last match_pair / match_batch call enqueued
+ * (host-side count, for benchmarking). */
+int serac_last_launch_count(void);
+
+/* Host-only view of the work schedule (no GPU needed): for `pairs` (pointers are
+ * used only to recognise shared images) and a persistent grid of `grid` CTAs
+ * (1..256), report the number of launch chunks, and for the first chunk the number
+ * of work items, the column splits per pair (out_nsplit[n_pairs of that chunk]) and
+ * the item ranges cta_first[grid + 1] (CTA c takes items [cta_first[c],
+ * cta_first[c+1])).  Any output may be NULL.  Returns SERAC_EINVAL on bad input. */
+int serac_schedule_describe(const serac_pair* pairs, int32_t n_pairs, int32_t grid, int32_t* out_chunks,
+                            int32_t* out_items, int32_t* out_nsplit, int32_t* cta_first);
+
+/* Static text for a status code. */
+const char* serac_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SERAC_H */

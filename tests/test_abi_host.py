@@ -1,0 +1,124 @@
+"""C ABI checks that need no GPU: the library loads, exports every symbol the header
+declares, and its host-only logic (parameters, workspace sizes, argument checks, the
+work schedule) behaves as documented.  No call here reaches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def serac():
+    from top_ratio_test_gb300 import _build
+    _build.build()
+    import top_ratio_test_gb300 as s
+    return s
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "serac.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(\w+)\s*\(", src, flags=re.M))
+
+
+def test_header_symbols_exported(serac):
+    names = _declared()
+    assert len(names) >= 10
+    assert names == set(serac.EXPORTS)
+    L = serac.lib()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(serac):
+    for s in (0, -1, -2, -3, -4, -5, -6):
+        assert serac.status_str(s) != "unknown status"
+    assert serac.status_str(7) == "unknown status"
+
+
+def test_default_params(serac):
+    p = serac.default_params(0.8, 0.7)
+    assert (p.ratio_num_sq, p.ratio_den_sq, p.norm_sq, p.min_score, p.mutual, p.col_ratio) == \
+        (16, 25, 262144, 200499, 1, 1)
+    p = serac.default_params(0.75, 0.7)
+    assert p.ratio_num_sq * 16 == p.ratio_den_sq * 9
+    q = serac.Params()
+    for bad in [(0.0, 0.7), (1.5, 0.7), (0.8, -0.1), (0.8, 2.0)]:
+        assert serac.lib().serac_default_params(ctypes.byref(q), *bad) == serac.EINVAL
+    assert serac.lib().serac_default_params(None, 0.8, 0.7) == serac.EINVAL
+
+
+def test_workspace_sizes(serac):
+    small = serac.pair_workspace_size(100, 100)
+    big = serac.pair_workspace_size(8192, 8192)
+    assert 0 < small < big
+    # 2 images x 8192 rows x 256 B staged, plus partials, well under 64 MiB
+    assert 8192 * 2 * 256 < big < 64 << 20
+    assert serac.pair_workspace_size(0, 0) > 0
+
+
+def test_bad_arguments_rejected_before_any_launch(serac):
+    L = serac.lib()
+    p = serac.default_params()
+    cnt = ctypes.c_int32()
+    out = serac._Out(16, 4, ctypes.addressof(cnt), None, None)
+    ws = 1 << 20
+    # null descriptors with n > 0
+    assert L.match_pair(None, 4, 16, 4, ctypes.byref(p), ctypes.byref(out), 256, ws, None) == serac.EINVAL
+    # negative size, size above the limit
+    assert L.match_pair(16, -1, 16, 4, ctypes.byref(p), ctypes.byref(out), 256, ws, None) == serac.EINVAL
+    assert L.match_pair(16, (1 << 24) + 1, 16, 4, ctypes.byref(p), ctypes.byref(out), 256, ws, None) == serac.EINVAL
+    # misaligned descriptors
+    assert L.match_pair(17, 4, 16, 4, ctypes.byref(p), ctypes.byref(out), 256, ws, None) == serac.EINVAL
+    # no params / no outputs / no count
+    assert L.match_pair(16, 4, 16, 4, None, ctypes.byref(out), 256, ws, None) == serac.EINVAL
+    assert L.match_pair(16, 4, 16, 4, ctypes.byref(p), None, 256, ws, None) == serac.EINVAL
+    out2 = serac._Out(16, 4, None, None, None)
+    assert L.match_pair(16, 4, 16, 4, ctypes.byref(p), ctypes.byref(out2), 256, ws, None) == serac.EINVAL
+    # misaligned optional top-2 output
+    out3 = serac._Out(16, 4, ctypes.addressof(cnt), 20, None)
+    assert L.match_pair(16, 4, 16, 4, ctypes.byref(p), ctypes.byref(out3), 256, ws, None) == serac.EINVAL
+    # ratio denominator must be positive
+    p0 = serac.default_params()
+    p0.ratio_den_sq = 0
+    assert L.match_pair(16, 4, 16, 4, ctypes.byref(p0), ctypes.byref(out), 256, ws, None) == serac.EINVAL
+    # batch: negative count, null arrays
+    assert L.match_batch(None, 2, ctypes.byref(p), None, 256, ws, None) == serac.EINVAL
+    assert L.match_batch(None, -1, ctypes.byref(p), None, 256, ws, None) == serac.EINVAL
+
+
+def test_schedule_covers_every_tile_once(serac):
+    # a single 8192 x 8192 pair on 152 CTAs
+    chunks, items, nsplit, first = serac.schedule_describe([(8192, 8192)], 152)
+    assert chunks == 1
+    assert nsplit == [19] and items == 64 * 19
+    assert first[0] == 0 and first[-1] == items
+    assert all(first[c] <= first[c + 1] for c in range(152))
+    # items go to the CTA holding their midpoint: loads differ by at most one tile here
+    cts = 32
+    per_item = [(s + 1) * cts // 19 - s * cts // 19 for s in range(19)] * 64
+    loads = [sum(per_item[first[c]:first[c + 1]]) for c in range(152)]
+    assert sum(loads) == 64 * 32
+    assert max(loads) - min(loads) <= 1
+
+
+def test_schedule_ragged_and_empty(serac):
+    sizes = [(1000, 16384), (0, 500), (257, 0), (129, 255), (16384, 1000)]
+    chunks, items, nsplit, first = serac.schedule_describe(sizes, 152)
+    assert nsplit[1] == 0 and nsplit[2] == 0
+    rt = [(na + 127) // 128 for na, _ in sizes]
+    ct = [(nb + 255) // 256 for _, nb in sizes]
+    assert all(1 <= nsplit[k] <= ct[k] for k in (0, 3, 4))
+    assert items == sum(rt[k] * nsplit[k] for k in range(5))
+    assert first[-1] == items and first[0] == 0
+
+
+def test_schedule_large_batch_chunks(serac):
+    sizes = [(8192, 8192)] * 300
+    chunks, items, nsplit, first = serac.schedule_describe(sizes, 152)
+    # 64 MiB of column partials per chunk -> 16 pairs of 8192 x 8192 per chunk
+    assert chunks == (300 + 15) // 16
+    assert nsplit[0] == 2 and items == 16 * 64 * 2

@@ -1,0 +1,238 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, bit-exact.
+
+Integer work, so the bar is equality everywhere: scores, row and column top-2
+(score and index), and match lists (order included).
+"""
+import numpy as np
+import pytest
+import torch
+
+import sift_synth as S
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def serac():
+    import top_ratio_test_gb300 as s
+    assert torch.cuda.is_available()
+    assert s.device_check() == s.OK, s.status_str(s.device_check())
+    return s
+
+
+def _dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def _run_pair(serac, a, b, params=None, capacity=None):
+    out = serac.match_pair(_dev(a), _dev(b), params, capacity=capacity, top2=True)
+    torch.cuda.synchronize()
+    return out
+
+
+def _oracle_params(oracle_mod, p):
+    return oracle_mod.Params(p.ratio_num_sq, p.ratio_den_sq, p.norm_sq, p.min_score, p.mutual, p.col_ratio)
+
+
+def _assert_pair(serac, oracle_mod, a, b, params=None):
+    p = params if params is not None else serac.default_params()
+    out = _run_pair(serac, a, b, p)
+    ref = oracle_mod.match(a, b, _oracle_params(oracle_mod, p))
+    na, nb = a.shape[0], b.shape[0]
+    np.testing.assert_array_equal(out.row_top2.cpu().numpy()[:na], ref.row_top2)
+    np.testing.assert_array_equal(out.col_top2.cpu().numpy()[:nb], ref.col_top2)
+    np.testing.assert_array_equal(out.result().numpy(), ref.matches)
+    return out, ref
+
+
+# ------------------------------------------------------------------ contraction
+
+def _adversarial(seed, na, nb):
+    rng = np.random.default_rng(seed)
+    a = rng.integers(0, 256, size=(na, 128)).astype(np.uint8)
+    b = rng.integers(0, 256, size=(nb, 128)).astype(np.uint8)
+    a[0] = 255                      # 8,323,200 against an all-255 row: the largest score
+    b[0] = 255
+    if na > 2:
+        a[1] = 0
+        a[1, 0] = 255               # one 255^2 product among zeros
+        a[2, ::2] = 255
+        a[2, 1::2] = 1
+    if nb > 2:
+        b[2] = 1                    # many 1 x k products
+    return a, b
+
+
+@pytest.mark.parametrize("na,nb", [(1, 1), (3, 300), (130, 257), (256, 512), (300, 700)])
+def test_scores_exact(serac, oracle_mod, na, nb):
+    a, b = _adversarial(na * 1000 + nb, na, nb)
+    s = serac.scores(_dev(a), _dev(b))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(s.cpu().numpy(), oracle_mod.scores(a, b))
+
+
+def test_fused_equals_unfused(serac, oracle_mod):
+    """Top-2 taken from the written-out score matrix equals the fused result."""
+    a, b = _adversarial(5, 200, 600)
+    a[10:20] = a[0]                 # duplicated rows and columns force ties
+    b[30:40] = b[3]
+    s = serac.scores(_dev(a), _dev(b)).cpu().numpy().astype(np.int64)
+    out = _run_pair(serac, a, b)
+
+    def top2(v):
+        idx = np.nonzero(v > 0)[0]
+        o = idx[np.lexsort((idx, -v[idx]))]
+        return [int(v[o[0]]) if len(o) else 0, int(o[0]) if len(o) else -1,
+                int(v[o[1]]) if len(o) > 1 else 0, int(o[1]) if len(o) > 1 else -1]
+
+    assert out.row_top2.cpu().numpy().tolist() == [top2(s[i]) for i in range(200)]
+    assert out.col_top2.cpu().numpy().tolist() == [top2(s[:, j]) for j in range(600)]
+
+
+# ------------------------------------------------------------------ single pairs
+
+def test_pair_2000(serac, oracle_mod):
+    p = S.single_pair_2000(0)
+    out, ref = _assert_pair(serac, oracle_mod, p.a, p.b)
+    got = {tuple(x) for x in out.result().numpy().tolist()}
+    assert got == {tuple(x) for x in p.truth.tolist()}
+
+
+def test_pair_8192(serac, oracle_mod):
+    p = S.single_pair_8192(0)
+    out, ref = _assert_pair(serac, oracle_mod, p.a, p.b)
+    assert len(ref.matches) > 1500
+
+
+@pytest.mark.parametrize("na,nb", [(0, 0), (0, 7), (7, 0), (1, 1), (1, 300), (127, 129), (128, 256),
+                                   (129, 255), (255, 257), (257, 1), (1000, 2300), (3001, 513)])
+def test_ragged_sizes(serac, oracle_mod, na, nb):
+    p = S.make_pair(1, 60, na * 7 + nb, na, nb, 0.3, 0.05)
+    _assert_pair(serac, oracle_mod, p.a, p.b)
+
+
+def test_largest_size(serac, oracle_mod):
+    p = S.make_pair(2, 61, 0, 16384, 16384, 0.15, 0.05)
+    _assert_pair(serac, oracle_mod, p.a, p.b)
+
+
+@pytest.mark.parametrize("variant", ["default", "no_col_ratio", "no_mutual", "loose"])
+def test_ties_and_params(serac, oracle_mod, variant):
+    rng = np.random.default_rng(11)
+    vals = np.array([0, 1, 2, 255], np.uint8)
+    a = vals[rng.integers(0, 4, size=(300, 128))]
+    b = vals[rng.integers(0, 4, size=(500, 128))]
+    a[rng.random(a.shape) < 0.7] = 0
+    b[rng.random(b.shape) < 0.7] = 0
+    a[150:160] = a[3]
+    b[200:230] = b[7]
+    b[499] = b[7]
+    p = serac.default_params()
+    if variant == "no_col_ratio":
+        p.col_ratio = 0
+    elif variant == "no_mutual":
+        p.mutual, p.col_ratio = 0, 0
+    elif variant == "loose":
+        p.norm_sq, p.min_score = 2_000_000, 0
+    _assert_pair(serac, oracle_mod, a, b, p)
+
+
+def test_capacity_overflow_and_repeat(serac, oracle_mod):
+    p = S.single_pair_2000(0)
+    ref = oracle_mod.match(p.a, p.b)
+    out = _run_pair(serac, p.a, p.b, capacity=100)
+    assert int(out.count.item()) == len(ref.matches)
+    np.testing.assert_array_equal(out.matches[:100].cpu().numpy(), ref.matches[:100])
+    with pytest.raises(serac.SeracError):
+        out.result()
+    # same inputs twice on one workspace: identical
+    a, b = _dev(p.a), _dev(p.b)
+    ws = serac.workspace(serac.pair_workspace_size(2000, 2000), a.device)
+    r1 = serac.match_pair(a, b, workspace_t=ws, top2=True)
+    r2 = serac.match_pair(a, b, workspace_t=ws, top2=True)
+    torch.cuda.synchronize()
+    assert torch.equal(r1.row_top2, r2.row_top2) and torch.equal(r1.col_top2, r2.col_top2)
+    assert torch.equal(r1.result(), r2.result())
+
+
+def test_workspace_too_small(serac):
+    a = torch.zeros((10, 128), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(serac.SeracError) as e:
+        serac.match_pair(a, a, workspace_t=ws)
+    assert e.value.status == serac.EWORKSPACE
+
+
+def test_same_image_both_sides(serac, oracle_mod):
+    p = S.make_pair(3, 62, 0, 700, 10, 0.0, 0.05)
+    a = _dev(p.a)
+    out = serac.match_pair(a, a, top2=True)
+    torch.cuda.synchronize()
+    ref = oracle_mod.match(p.a, p.a)
+    np.testing.assert_array_equal(out.row_top2.cpu().numpy(), ref.row_top2)
+    np.testing.assert_array_equal(out.result().numpy(), ref.matches)
+
+
+# ------------------------------------------------------------------ batches
+
+def test_batch_ring_12(serac, oracle_mod):
+    """12 images x 8,192, all 66 pairs through match_batch, every pair in full."""
+    r = S.ring_12x8192(0)
+    imgs = [_dev(x) for x in r.images]
+    outs = serac.match_batch([(imgs[i], imgs[j]) for i, j in r.pairs], top2=True)
+    torch.cuda.synchronize()
+    for k, (i, j) in enumerate(r.pairs):
+        ref = oracle_mod.match(r.images[i], r.images[j])
+        np.testing.assert_array_equal(outs[k].row_top2.cpu().numpy(), ref.row_top2)
+        np.testing.assert_array_equal(outs[k].col_top2.cpu().numpy(), ref.col_top2)
+        np.testing.assert_array_equal(outs[k].result().numpy(), ref.matches)
+
+
+def test_batch_ragged_256(serac, oracle_mod):
+    """256 ragged pairs (1,000..16,384 features): 12 pairs checked in full, every
+    pair checked on 48 sampled rows (top-2 and decision) and 48 sampled columns."""
+    sizes = S.ragged_sizes(0)
+    pairs = [S.ragged_pair(0, k, sizes) for k in range(256)]
+    dev = [(_dev(p.a), _dev(p.b)) for p in pairs]
+    outs = serac.match_batch(dev, top2=True)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    full = set(rng.choice(256, 12, replace=False).tolist())
+    par = oracle_mod.Params()
+    for k, p in enumerate(pairs):
+        o = outs[k]
+        rows_t = o.row_top2.cpu().numpy()
+        cols_t = o.col_top2.cpu().numpy()
+        m = o.result().numpy()
+        if k in full:
+            ref = oracle_mod.match(p.a, p.b)
+            np.testing.assert_array_equal(rows_t, ref.row_top2)
+            np.testing.assert_array_equal(cols_t, ref.col_top2)
+            np.testing.assert_array_equal(m, ref.matches)
+            continue
+        ri = rng.choice(p.a.shape[0], 48, replace=False).astype(np.int32)
+        cj = rng.choice(p.b.shape[0], 48, replace=False).astype(np.int32)
+        j, rt, _ = oracle_mod.accept_rows(p.a, p.b, ri, par)
+        np.testing.assert_array_equal(rows_t[ri], rt)
+        np.testing.assert_array_equal(cols_t[cj], oracle_mod.col_top2(p.a, p.b, cj))
+        kept = dict(zip(m[:, 0].tolist(), m[:, 1].tolist()))
+        assert [kept.get(int(i), -1) for i in ri] == j.tolist()
+        assert np.all(np.diff(m[:, 0]) > 0)
+
+
+def test_batch_survey_spot_50(serac, oracle_mod):
+    """100 images x 8,192 (4,950 pairs) through match_batch; the 50 seeded pairs
+    are checked in full against the oracle, every pair for order and range."""
+    r = S.survey_100x8192(0)
+    imgs = [_dev(x) for x in r.images]
+    outs = serac.match_batch([(imgs[i], imgs[j]) for i, j in r.pairs])
+    torch.cuda.synchronize()
+    counts = torch.cat([o.count for o in outs]).cpu().numpy()
+    assert counts.min() >= 0 and counts.max() <= 8192
+    for k in S.survey_spot_pairs(0).tolist():
+        i, j = r.pairs[k]
+        ref = oracle_mod.match(r.images[i], r.images[j])
+        np.testing.assert_array_equal(outs[k].result().numpy(), ref.matches)
+    # planted neighbours match, far pairs (ring distance > 3) almost never do
+    near = [k for k, (i, j) in enumerate(r.pairs) if min((j - i) % 100, (i - j) % 100) <= 3]
+    assert counts[near].min() > 500

@@ -1,0 +1,242 @@
+"""Python binding of libserac_gb300.so: exhaustive SIFT descriptor matching with a
+fused top-2 on GB300 (sm_103a).
+
+This module only marshals arguments for the C ABI declared in ``include/serac.h``;
+every step of the matching runs in the library's CUDA kernels.  PyTorch supplies the
+device memory (inputs, outputs, workspace) and the stream.  There is no fallback: if
+the library is missing or the GPU is not an sm_103 part, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libserac_gb300.so")
+
+OK, EINVAL, ECAPACITY, ECUDA, ETIMEOUT, EWORKSPACE, EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
+DIM = 128
+
+# every symbol include/serac.h declares
+EXPORTS = ("serac_default_params", "serac_pair_workspace_size", "match_pair",
+           "match_batch_workspace_size", "match_batch", "serac_scores",
+           "serac_set_profile_events", "serac_device_check", "serac_last_launch_count",
+           "serac_schedule_describe", "serac_status_str")
+
+
+class SeracError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_str(status)} ({status})" if what else status_str(status))
+
+
+class Params(ctypes.Structure):
+    _fields_ = [("ratio_num_sq", ctypes.c_int32), ("ratio_den_sq", ctypes.c_int32),
+                ("norm_sq", ctypes.c_int32), ("min_score", ctypes.c_int32),
+                ("mutual", ctypes.c_int32), ("col_ratio", ctypes.c_int32)]
+
+    def __repr__(self):
+        return ("Params(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")")
+
+
+class _Pair(ctypes.Structure):
+    _fields_ = [("a", ctypes.c_void_p), ("n_a", ctypes.c_int32),
+                ("b", ctypes.c_void_p), ("n_b", ctypes.c_int32)]
+
+
+class _Out(ctypes.Structure):
+    _fields_ = [("matches", ctypes.c_void_p), ("capacity", ctypes.c_int32),
+                ("count", ctypes.c_void_p), ("row_top2", ctypes.c_void_p),
+                ("col_top2", ctypes.c_void_p)]
+
+
+_lib_handle = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(_LIB_PATH)
+        P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        L.serac_default_params.argtypes = [ctypes.POINTER(Params), ctypes.c_float, ctypes.c_float]
+        L.serac_pair_workspace_size.argtypes = [i32, i32]
+        L.serac_pair_workspace_size.restype = sz
+        L.match_pair.argtypes = [P, i32, P, i32, ctypes.POINTER(Params), ctypes.POINTER(_Out), P, sz, P]
+        L.match_batch_workspace_size.argtypes = [ctypes.POINTER(_Pair), i32]
+        L.match_batch_workspace_size.restype = sz
+        L.match_batch.argtypes = [ctypes.POINTER(_Pair), i32, ctypes.POINTER(Params),
+                                  ctypes.POINTER(_Out), P, sz, P]
+        L.serac_scores.argtypes = [P, i32, P, i32, P, P, sz, P]
+        L.serac_set_profile_events.argtypes = [P, P]
+        L.serac_schedule_describe.argtypes = [ctypes.POINTER(_Pair), i32, i32, P, P, P, P]
+        L.serac_status_str.restype = ctypes.c_char_p
+        _lib_handle = L
+    return _lib_handle
+
+
+def status_str(status: int) -> str:
+    return lib().serac_status_str(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != OK:
+        raise SeracError(status, what)
+
+
+def default_params(max_ratio: float = 0.8, max_angle: float = 0.7, mutual: int = 1,
+                   col_ratio: int = 1) -> Params:
+    p = Params()
+    _check(lib().serac_default_params(ctypes.byref(p), max_ratio, max_angle), "serac_default_params")
+    p.mutual, p.col_ratio = int(mutual), int(col_ratio)
+    return p
+
+
+def device_check() -> int:
+    return int(lib().serac_device_check())
+
+
+def last_launch_count() -> int:
+    return int(lib().serac_last_launch_count())
+
+
+def set_profile_events(begin: Optional[torch.cuda.Event], end: Optional[torch.cuda.Event]) -> None:
+    lib().serac_set_profile_events(begin.cuda_event if begin is not None else None,
+                                   end.cuda_event if end is not None else None)
+
+
+def pair_workspace_size(n_a: int, n_b: int) -> int:
+    return int(lib().serac_pair_workspace_size(int(n_a), int(n_b)))
+
+
+def _desc(x: torch.Tensor, name: str) -> torch.Tensor:
+    if x.dtype != torch.uint8 or x.dim() != 2 or x.shape[1] != DIM or not x.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA uint8 tensor of shape (n, {DIM})")
+    if not x.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return x
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """Caller-owned device scratch (256-byte aligned by the caching allocator)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+@dataclass
+class MatchOutput:
+    """Device outputs of one pair.  `count` holds the number of matches (or a negative
+    status); `matches` has room for `capacity` rows of (i, j), ascending i."""
+    matches: torch.Tensor
+    count: torch.Tensor
+    row_top2: Optional[torch.Tensor]
+    col_top2: Optional[torch.Tensor]
+
+    def result(self):
+        """Synchronise and return the matches as a (count, 2) int32 CPU tensor."""
+        n = int(self.count.item())
+        if n < 0:
+            raise SeracError(n, "match")
+        if n > self.matches.shape[0]:
+            raise SeracError(ECAPACITY, f"match ({n} matches, capacity {self.matches.shape[0]})")
+        return self.matches[:n].cpu()
+
+
+def _make_out(n_a: int, n_b: int, device, capacity: Optional[int], top2: bool):
+    cap = n_a if capacity is None else int(capacity)
+    o = MatchOutput(matches=torch.empty((max(cap, 1), 2), dtype=torch.int32, device=device),
+                    count=torch.empty(1, dtype=torch.int32, device=device),
+                    row_top2=torch.empty((max(n_a, 1), 4), dtype=torch.int32, device=device) if top2 else None,
+                    col_top2=torch.empty((max(n_b, 1), 4), dtype=torch.int32, device=device) if top2 else None)
+    c = _Out(o.matches.data_ptr(), cap, o.count.data_ptr(),
+             o.row_top2.data_ptr() if top2 else None, o.col_top2.data_ptr() if top2 else None)
+    return o, c
+
+
+def match_pair(a: torch.Tensor, b: torch.Tensor, params: Optional[Params] = None, *,
+               capacity: Optional[int] = None, top2: bool = False,
+               workspace_t: Optional[torch.Tensor] = None, stream=None) -> MatchOutput:
+    """Match descriptors a (n_a, 128) against b (n_b, 128), asynchronously."""
+    a, b = _desc(a, "a"), _desc(b, "b")
+    p = params if params is not None else default_params()
+    n_a, n_b = a.shape[0], b.shape[0]
+    need = pair_workspace_size(n_a, n_b)
+    ws = workspace_t if workspace_t is not None else workspace(need, a.device)
+    o, c = _make_out(n_a, n_b, a.device, capacity, top2)
+    st = lib().match_pair(a.data_ptr(), n_a, b.data_ptr(), n_b, ctypes.byref(p), ctypes.byref(c),
+                          ws.data_ptr(), ws.numel(), _stream_ptr(stream))
+    _check(st, "match_pair")
+    return o
+
+
+def _pairs_struct(pairs: Sequence):
+    arr = (_Pair * max(len(pairs), 1))()
+    for k, (a, b) in enumerate(pairs):
+        _desc(a, f"pairs[{k}].a")
+        _desc(b, f"pairs[{k}].b")
+        arr[k] = _Pair(a.data_ptr(), a.shape[0], b.data_ptr(), b.shape[0])
+    return arr
+
+
+def batch_workspace_size(pairs: Sequence) -> int:
+    arr = _pairs_struct(pairs)
+    return int(lib().match_batch_workspace_size(arr, len(pairs)))
+
+
+def match_batch(pairs: Sequence, params: Optional[Params] = None, *, capacities=None,
+                top2: bool = False, workspace_t: Optional[torch.Tensor] = None,
+                stream=None) -> list:
+    """Match every (a, b) of `pairs`; images shared between pairs are staged once."""
+    arr = _pairs_struct(pairs)
+    p = params if params is not None else default_params()
+    n = len(pairs)
+    need = int(lib().match_batch_workspace_size(arr, n))
+    dev = pairs[0][0].device if n else torch.device("cuda")
+    ws = workspace_t if workspace_t is not None else workspace(need, dev)
+    outs, couts = [], (_Out * max(n, 1))()
+    for k, (a, b) in enumerate(pairs):
+        cap = None if capacities is None else capacities[k]
+        o, c = _make_out(a.shape[0], b.shape[0], a.device, cap, top2)
+        outs.append(o)
+        couts[k] = c
+    st = lib().match_batch(arr, n, ctypes.byref(p), couts, ws.data_ptr(), ws.numel(), _stream_ptr(stream))
+    _check(st, "match_batch")
+    return outs
+
+
+def scores(a: torch.Tensor, b: torch.Tensor, *, workspace_t: Optional[torch.Tensor] = None,
+           stream=None) -> torch.Tensor:
+    """Full (n_a, n_b) int32 score matrix from the same tensor-core tiles (small n)."""
+    a, b = _desc(a, "a"), _desc(b, "b")
+    n_a, n_b = a.shape[0], b.shape[0]
+    out = torch.empty((max(n_a, 1), max(n_b, 1)), dtype=torch.int32, device=a.device)
+    ws = workspace_t if workspace_t is not None else workspace(pair_workspace_size(n_a, n_b), a.device)
+    st = lib().serac_scores(a.data_ptr(), n_a, b.data_ptr(), n_b, out.data_ptr(), ws.data_ptr(),
+                            ws.numel(), _stream_ptr(stream))
+    _check(st, "serac_scores")
+    return out[:n_a, :n_b]
+
+
+def schedule_describe(sizes: Sequence, grid: int):
+    """Host-side view of how the first launch chunk of pairs with these (n_a, n_b)
+    sizes is cut: (chunks, items, nsplit per pair, cta_first[grid + 1])."""
+    n = len(sizes)
+    arr = (_Pair * max(n, 1))()
+    for k, (na, nb) in enumerate(sizes):
+        arr[k] = _Pair(16 * (2 * k + 1), int(na), 16 * (2 * k + 2), int(nb))
+    chunks, items = ctypes.c_int32(), ctypes.c_int32()
+    nsplit = (ctypes.c_int32 * max(n, 1))()
+    first = (ctypes.c_int32 * (grid + 1))()
+    _check(lib().serac_schedule_describe(arr, n, grid, ctypes.byref(chunks), ctypes.byref(items),
+                                         nsplit, first), "serac_schedule_describe")
+    return chunks.value, items.value, list(nsplit)[:n], list(first)

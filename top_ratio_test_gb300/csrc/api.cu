@@ -1,0 +1,525 @@
+// C ABI of libserac_gb300: argument checks, image staging plan, workspace layout,
+// the work-item schedule of the persistent fused kernel, and the launch sequence.
+//
+// Schedule.  Pairs are processed in launch chunks of at most MAX_PAIRS pairs (the
+// per-pair tables travel as kernel parameters, so a call needs no host-to-device
+// copy and can be captured in a CUDA graph).  Within a chunk every pair is cut into
+// work items (row tile x column split); the split count is chosen so the chunk has
+// at least ~8 items per SM of a 152-SM GB300, and items are handed to the
+// persistent CTAs as contiguous ranges of equal tile count.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <utility>
+#include <vector>
+
+#include "serac.h"
+#include "serac_internal.h"
+
+namespace serac {
+namespace {
+
+constexpr int TARGET_CTAS = 152;            // SMs of a GB300; fixes the item cut
+constexpr int ITEMS_PER_CTA = 8;
+constexpr int64_t CHUNK_COLPART_BYTES = 64ll << 20;
+constexpr size_t ALIGN = 1024;
+
+size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
+
+struct Chunk {
+  int p0 = 0, p1 = 0;          // pairs [p0, p1)
+  int nsplit_target = 1;
+  int64_t items = 0;
+  int64_t colpart = 0;         // entries
+  int64_t rows = 0, cols = 0;  // sum of n_a, n_b
+};
+
+struct Plan {
+  std::vector<StageImage> images;  // unique images with their staged row offsets
+  std::vector<int> a_img, b_img;   // per pair
+  int64_t staged_rows = 0;
+  std::vector<Chunk> chunks;
+  size_t off_err = 0, off_staged = 0, off_rowpart = 0, off_colpart = 0, off_rowfinal = 0, off_colfinal = 0;
+  size_t total = 0;
+};
+
+int64_t row_tiles(int32_t n_a) { return (static_cast<int64_t>(n_a) + BM - 1) / BM; }
+int64_t col_tiles(int32_t n_b) { return (static_cast<int64_t>(n_b) + BN - 1) / BN; }
+
+int pair_nsplit(const serac_pair& pr, int target) {
+  if (pr.n_a <= 0 || pr.n_b <= 0) return 0;
+  return static_cast<int>(std::min<int64_t>(target, col_tiles(pr.n_b)));
+}
+
+void build_plan(const serac_pair* pairs, int32_t n_pairs, Plan& pl) {
+  std::map<std::pair<const uint8_t*, int32_t>, int> seen;
+  auto image_of = [&](const uint8_t* ptr, int32_t n) {
+    auto key = std::make_pair(ptr, n);
+    auto it = seen.find(key);
+    if (it != seen.end()) return it->second;
+    const int idx = static_cast<int>(pl.images.size());
+    StageImage im;
+    im.src = ptr;
+    im.n = n;
+    im.row0 = static_cast<int32_t>(pl.staged_rows);
+    pl.staged_rows += round_up(n, PAD_ROWS);
+    pl.images.push_back(im);
+    seen.emplace(key, idx);
+    return idx;
+  };
+  pl.a_img.resize(n_pairs);
+  pl.b_img.resize(n_pairs);
+  for (int p = 0; p < n_pairs; ++p) {
+    pl.a_img[p] = image_of(pairs[p].a, pairs[p].n_a);
+    pl.b_img[p] = image_of(pairs[p].b, pairs[p].n_b);
+  }
+  // chunks of consecutive pairs
+  int p = 0;
+  while (p < n_pairs || (n_pairs == 0 && pl.chunks.empty())) {
+    Chunk ch;
+    ch.p0 = p;
+    int64_t colpart = 0;
+    while (p < n_pairs && p - ch.p0 < MAX_PAIRS) {
+      const int64_t cp = row_tiles(pairs[p].n_a) * round_up(pairs[p].n_b, PAD_ROWS);
+      if (p > ch.p0 && (colpart + cp) * 8 > CHUNK_COLPART_BYTES) break;
+      colpart += cp;
+      ++p;
+    }
+    ch.p1 = p;
+    int64_t rtt = 0;
+    for (int k = ch.p0; k < ch.p1; ++k)
+      if (pairs[k].n_a > 0 && pairs[k].n_b > 0) rtt += row_tiles(pairs[k].n_a);
+    ch.nsplit_target = rtt > 0 ? static_cast<int>(std::max<int64_t>(
+                                     1, (static_cast<int64_t>(ITEMS_PER_CTA) * TARGET_CTAS + rtt - 1) / rtt))
+                               : 1;
+    for (int k = ch.p0; k < ch.p1; ++k) {
+      const int ns = pair_nsplit(pairs[k], ch.nsplit_target);
+      ch.items += row_tiles(pairs[k].n_a) * ns;
+      if (ns > 0) ch.colpart += row_tiles(pairs[k].n_a) * round_up(pairs[k].n_b, PAD_ROWS);
+      ch.rows += pairs[k].n_a;
+      ch.cols += pairs[k].n_b;
+    }
+    pl.chunks.push_back(ch);
+    if (n_pairs == 0) break;
+  }
+  int64_t max_items = 0, max_colpart = 0, max_rows = 0, max_cols = 0;
+  for (const Chunk& ch : pl.chunks) {
+    max_items = std::max(max_items, ch.items);
+    max_colpart = std::max(max_colpart, ch.colpart);
+    max_rows = std::max(max_rows, ch.rows);
+    max_cols = std::max(max_cols, ch.cols);
+  }
+  size_t off = 0;
+  pl.off_err = off;
+  off = align_up(off + 256);
+  pl.off_staged = off;
+  off = align_up(off + static_cast<size_t>(pl.staged_rows) * KDIM * 2);
+  pl.off_rowpart = off;
+  off = align_up(off + static_cast<size_t>(max_items) * 2 * BM * sizeof(ulonglong2));
+  pl.off_colpart = off;
+  off = align_up(off + static_cast<size_t>(max_colpart) * sizeof(uint2));
+  pl.off_rowfinal = off;
+  off = align_up(off + static_cast<size_t>(max_rows) * sizeof(int4));
+  pl.off_colfinal = off;
+  off = align_up(off + static_cast<size_t>(max_cols) * sizeof(int4));
+  pl.total = off;
+}
+
+// Contiguous item ranges of equal tile count: item i, covering tiles
+// [Q_i, Q_i + w_i) of C, goes to the CTA its midpoint falls in,
+// floor((2 Q_i + w_i) * G / 2C).
+void cut_items(const serac_pair* pairs, const Chunk& ch, int grid, int32_t* cta_first) {
+  const int64_t total_items = ch.items;
+  int64_t total_cost = 0;
+  for (int k = ch.p0; k < ch.p1; ++k)
+    if (pair_nsplit(pairs[k], ch.nsplit_target) > 0) total_cost += row_tiles(pairs[k].n_a) * col_tiles(pairs[k].n_b);
+  for (int c = 0; c <= grid; ++c) cta_first[c] = static_cast<int32_t>(total_items);
+  int64_t item = 0, q = 0;
+  int next_cta = 0;
+  for (int k = ch.p0; k < ch.p1; ++k) {
+    const int ns = pair_nsplit(pairs[k], ch.nsplit_target);
+    if (ns == 0) continue;
+    const int64_t rts = row_tiles(pairs[k].n_a), cts = col_tiles(pairs[k].n_b);
+    for (int64_t rt = 0; rt < rts; ++rt) {
+      for (int s = 0; s < ns; ++s, ++item) {
+        const int64_t w = (s + 1) * cts / ns - s * cts / ns;
+        int c = static_cast<int>(total_cost > 0 ? (2 * q + w) * grid / (2 * total_cost) : 0);
+        if (c > grid - 1) c = grid - 1;
+        while (next_cta <= c) cta_first[next_cta++] = static_cast<int32_t>(item);
+        q += w;
+      }
+    }
+  }
+  while (next_cta <= grid) cta_first[next_cta++] = static_cast<int32_t>(total_items);
+}
+
+// ------------------------------------------------------------------ device state
+struct DeviceInfo {
+  bool init = false;
+  int ok = 0;
+  int sms = 0;
+};
+DeviceInfo g_dev[64];
+
+int device_info(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SERAC_ECUDA;
+  if (dev < 0 || dev >= 64) return SERAC_EUNSUPPORTED;
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SERAC_ECUDA;
+    d.ok = (major == 10 && minor == 3) ? 1 : 0;
+    d.sms = n;
+    d.init = true;
+  }
+  if (!d.ok) return SERAC_EUNSUPPORTED;
+  *sms = d.sms;
+  return SERAC_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// One tensor map over the whole staged buffer: [rows][128] bf16, box 64 x 128,
+// 128-byte swizzle (the layout the MMA's shared-memory descriptors describe).
+int encode_staged_map(CUtensorMap* map, void* staged, int64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return SERAC_EUNSUPPORTED;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(KDIM), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(KDIM) * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, staged, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SERAC_OK : SERAC_ECUDA;
+}
+
+cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
+int g_last_launches = 0;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_pairs(const serac_pair* pairs, int32_t n_pairs) {
+  if (n_pairs < 0 || (n_pairs > 0 && !pairs)) return SERAC_EINVAL;
+  for (int p = 0; p < n_pairs; ++p) {
+    const serac_pair& pr = pairs[p];
+    if (pr.n_a < 0 || pr.n_b < 0 || pr.n_a > SERAC_MAX_N || pr.n_b > SERAC_MAX_N) return SERAC_EINVAL;
+    if ((pr.n_a > 0 && (!pr.a || !aligned(pr.a, 16))) || (pr.n_b > 0 && (!pr.b || !aligned(pr.b, 16))))
+      return SERAC_EINVAL;
+  }
+  return SERAC_OK;
+}
+
+int check_params(const serac_params* p) {
+  if (!p) return SERAC_EINVAL;
+  if (p->ratio_num_sq < 0 || p->ratio_den_sq <= 0) return SERAC_EINVAL;
+  return SERAC_OK;
+}
+
+int check_out(const serac_out* o, int32_t n_a, int32_t n_b) {
+  if (!o || !o->count || !aligned(o->count, 4) || o->capacity < 0) return SERAC_EINVAL;
+  if (o->capacity > 0 && (!o->matches || !aligned(o->matches, 8))) return SERAC_EINVAL;
+  if (o->row_top2 && !aligned(o->row_top2, 16)) return SERAC_EINVAL;
+  if (o->col_top2 && !aligned(o->col_top2, 16)) return SERAC_EINVAL;
+  (void)n_a;
+  (void)n_b;
+  return SERAC_OK;
+}
+
+#define SERAC_TRY_CUDA(x)                              \
+  do {                                                 \
+    if ((x) != cudaSuccess) return SERAC_ECUDA;        \
+  } while (0)
+
+// The whole sequence: staging, then per chunk fused -> reduce -> match (or the
+// score dump when `dump` is set).
+int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, const serac_out* outs,
+        int32_t* dump, void* workspace, size_t ws_bytes, void* stream) {
+  g_last_launches = 0;
+  int sms = 0;
+  int st = device_info(&sms);
+  if (st != SERAC_OK) return st;
+  Plan pl;
+  build_plan(pairs, n_pairs, pl);
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < pl.total) return SERAC_EWORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* err = reinterpret_cast<int32_t*>(ws + pl.off_err);
+  uint16_t* staged = reinterpret_cast<uint16_t*>(ws + pl.off_staged);
+
+  CUtensorMap map;
+  if (pl.staged_rows > 0) {
+    st = encode_staged_map(&map, staged, pl.staged_rows);
+    if (st != SERAC_OK) return st;
+  }
+  SERAC_TRY_CUDA(cudaMemsetAsync(err, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)));
+
+  // staging, 512 images per launch
+  for (size_t i0 = 0; i0 < pl.images.size(); i0 += 512) {
+    StageParams sp;
+    sp.n_images = 0;
+    sp.max_pad_rows = 0;
+    sp.staged = staged;
+    int64_t max_chunks = 0;
+    for (size_t i = i0; i < pl.images.size() && i < i0 + 512; ++i) {
+      if (pl.images[i].n == 0) continue;
+      sp.images[sp.n_images++] = pl.images[i];
+      max_chunks = std::max<int64_t>(max_chunks, round_up(pl.images[i].n, PAD_ROWS) * (KDIM / 16));
+    }
+    if (sp.n_images == 0) continue;
+    if (launch_stage(sp, max_chunks, stream) != 0) return SERAC_ECUDA;
+    ++g_last_launches;
+  }
+
+  bool first_fused = true;
+  for (const Chunk& ch : pl.chunks) {
+    // ---------------- fused GEMM + top-2
+    if (ch.items > 0) {
+      FusedParams fp;
+      std::memset(&fp, 0, sizeof(fp));
+      fp.grid = static_cast<int32_t>(std::min<int64_t>({static_cast<int64_t>(sms), ch.items, MAX_GRID}));
+      fp.n_items = static_cast<int32_t>(ch.items);
+      fp.colpart = reinterpret_cast<uint2*>(ws + pl.off_colpart);
+      fp.rowpart = reinterpret_cast<ulonglong2*>(ws + pl.off_rowpart);
+      fp.err = err;
+      fp.dump = dump;
+      fp.dump_ld = (dump && n_pairs > 0) ? pairs[0].n_b : 0;
+      int np = 0;
+      int64_t item_base = 0, colpart_base = 0;
+      for (int k = ch.p0; k < ch.p1; ++k) {
+        const int ns = pair_nsplit(pairs[k], ch.nsplit_target);
+        if (ns == 0) continue;
+        FusedPair& f = fp.pairs[np++];
+        f.a_row0 = pl.images[pl.a_img[k]].row0;
+        f.b_row0 = pl.images[pl.b_img[k]].row0;
+        f.n_a = pairs[k].n_a;
+        f.n_b = pairs[k].n_b;
+        f.nsplit = ns;
+        f.item_base = static_cast<int32_t>(item_base);
+        f.colpart_base = colpart_base;
+        item_base += row_tiles(pairs[k].n_a) * ns;
+        colpart_base += row_tiles(pairs[k].n_a) * round_up(pairs[k].n_b, PAD_ROWS);
+      }
+      fp.n_pairs = np;
+      cut_items(pairs, ch, fp.grid, fp.cta_first);
+      const bool prof = first_fused && g_ev_begin && g_ev_end;
+      if (prof)
+        SERAC_TRY_CUDA(cudaEventRecordWithFlags(g_ev_begin, static_cast<cudaStream_t>(stream), cudaEventRecordExternal));
+      if (launch_fused(fp, &map, dump != nullptr, stream) != 0) return SERAC_ECUDA;
+      ++g_last_launches;
+      if (prof)
+        SERAC_TRY_CUDA(cudaEventRecordWithFlags(g_ev_end, static_cast<cudaStream_t>(stream), cudaEventRecordExternal));
+      first_fused = false;
+    }
+    if (dump) continue;
+    // ---------------- reduce + match
+    FinishParams fn;
+    std::memset(&fn, 0, sizeof(fn));
+    fn.ratio_num_sq = params->ratio_num_sq;
+    fn.ratio_den_sq = params->ratio_den_sq;
+    fn.norm_sq = params->norm_sq;
+    fn.min_score = params->min_score;
+    fn.mutual = params->mutual;
+    fn.col_ratio = params->col_ratio;
+    fn.colpart = reinterpret_cast<const uint2*>(ws + pl.off_colpart);
+    fn.rowpart = reinterpret_cast<const ulonglong2*>(ws + pl.off_rowpart);
+    fn.rowfinal = reinterpret_cast<int4*>(ws + pl.off_rowfinal);
+    fn.colfinal = reinterpret_cast<int4*>(ws + pl.off_colfinal);
+    fn.err = err;
+    int64_t item_base = 0, colpart_base = 0, rows = 0, cols = 0;
+    int np = 0;
+    for (int k = ch.p0; k < ch.p1; ++k) {
+      const int ns = pair_nsplit(pairs[k], ch.nsplit_target);
+      FinishPair& f = fn.pairs[np++];
+      f.n_a = pairs[k].n_a;
+      f.n_b = pairs[k].n_b;
+      f.nsplit = ns;
+      f.item_base = static_cast<int32_t>(item_base);
+      f.colpart_base = colpart_base;
+      f.row_base = static_cast<int32_t>(rows);
+      f.col_base = static_cast<int32_t>(cols);
+      f.matches = outs[k].matches;
+      f.count = outs[k].count;
+      f.row_top2 = outs[k].row_top2;
+      f.col_top2 = outs[k].col_top2;
+      f.capacity = outs[k].capacity;
+      if (ns > 0) {
+        item_base += row_tiles(pairs[k].n_a) * ns;
+        colpart_base += row_tiles(pairs[k].n_a) * round_up(pairs[k].n_b, PAD_ROWS);
+      }
+      rows += pairs[k].n_a;
+      cols += pairs[k].n_b;
+    }
+    fn.n_pairs = np;
+    fn.total_rows = static_cast<int32_t>(rows);
+    fn.total_cols = static_cast<int32_t>(cols);
+    if (rows + cols > 0) {
+      if (launch_reduce(fn, stream) != 0) return SERAC_ECUDA;
+      ++g_last_launches;
+    }
+    if (np > 0) {
+      if (launch_match(fn, stream) != 0) return SERAC_ECUDA;
+      ++g_last_launches;
+    }
+  }
+  return SERAC_OK;
+}
+
+}  // namespace
+}  // namespace serac
+
+using namespace serac;
+
+extern "C" {
+
+int serac_default_params(serac_params* p, float max_ratio, float max_angle_rad) {
+  if (!p || !(max_ratio > 0.0f) || max_ratio > 1.0f || !(max_angle_rad >= 0.0f) ||
+      max_angle_rad > 1.5707964f)
+    return SERAC_EINVAL;
+  const int64_t r = static_cast<int64_t>(std::llround(static_cast<double>(max_ratio) * 10000.0));
+  int64_t num = r * r, den = 100000000;
+  int64_t a = num, b = den;
+  while (b) {
+    const int64_t t = a % b;
+    a = b;
+    b = t;
+  }
+  num /= a;
+  den /= a;
+  const int32_t n = 512 * 512;
+  p->ratio_num_sq = static_cast<int32_t>(num);
+  p->ratio_den_sq = static_cast<int32_t>(den);
+  p->norm_sq = n;
+  p->min_score = static_cast<int32_t>(std::ceil(std::cos(static_cast<double>(max_angle_rad)) * n));
+  p->mutual = 1;
+  p->col_ratio = 1;
+  return SERAC_OK;
+}
+
+size_t serac_pair_workspace_size(int32_t n_a, int32_t n_b) {
+  serac_pair pr;
+  pr.a = reinterpret_cast<const uint8_t*>(16);
+  pr.b = reinterpret_cast<const uint8_t*>(32);
+  pr.n_a = n_a < 0 ? 0 : n_a;
+  pr.n_b = n_b < 0 ? 0 : n_b;
+  Plan pl;
+  build_plan(&pr, 1, pl);
+  return pl.total;
+}
+
+size_t match_batch_workspace_size(const serac_pair* pairs, int32_t n_pairs) {
+  if (check_pairs(pairs, n_pairs) != SERAC_OK) return 0;
+  Plan pl;
+  build_plan(pairs, n_pairs, pl);
+  return pl.total;
+}
+
+int match_pair(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b, int32_t n_b,
+               const serac_params* params, const serac_out* out, void* workspace, size_t workspace_bytes,
+               void* cuda_stream) {
+  serac_pair pr;
+  pr.a = desc_a;
+  pr.n_a = n_a;
+  pr.b = desc_b;
+  pr.n_b = n_b;
+  int st = check_pairs(&pr, 1);
+  if (st == SERAC_OK) st = check_params(params);
+  if (st == SERAC_OK) st = check_out(out, n_a, n_b);
+  if (st != SERAC_OK) return st;
+  return run(&pr, 1, params, out, nullptr, workspace, workspace_bytes, cuda_stream);
+}
+
+int match_batch(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, const serac_out* outs,
+                void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  int st = check_pairs(pairs, n_pairs);
+  if (st == SERAC_OK) st = check_params(params);
+  if (st != SERAC_OK) return st;
+  if (n_pairs > 0 && !outs) return SERAC_EINVAL;
+  for (int p = 0; p < n_pairs; ++p) {
+    st = check_out(&outs[p], pairs[p].n_a, pairs[p].n_b);
+    if (st != SERAC_OK) return st;
+  }
+  return run(pairs, n_pairs, params, outs, nullptr, workspace, workspace_bytes, cuda_stream);
+}
+
+int serac_scores(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b, int32_t n_b, int32_t* scores,
+                 void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  serac_pair pr;
+  pr.a = desc_a;
+  pr.n_a = n_a;
+  pr.b = desc_b;
+  pr.n_b = n_b;
+  int st = check_pairs(&pr, 1);
+  if (st != SERAC_OK) return st;
+  if (static_cast<int64_t>(n_a) * n_b > 0 && (!scores || !aligned(scores, 4))) return SERAC_EINVAL;
+  serac_params dummy;
+  serac_default_params(&dummy, 0.8f, 0.7f);
+  return run(&pr, 1, &dummy, nullptr, scores ? scores : reinterpret_cast<int32_t*>(16), workspace,
+             workspace_bytes, cuda_stream);
+}
+
+int serac_set_profile_events(void* ev_begin, void* ev_end) {
+  g_ev_begin = static_cast<cudaEvent_t>(ev_begin);
+  g_ev_end = static_cast<cudaEvent_t>(ev_end);
+  return SERAC_OK;
+}
+
+int serac_device_check(void) {
+  int sms = 0;
+  return device_info(&sms);
+}
+
+int serac_last_launch_count(void) { return g_last_launches; }
+
+int serac_schedule_describe(const serac_pair* pairs, int32_t n_pairs, int32_t grid, int32_t* out_chunks,
+                            int32_t* out_items, int32_t* out_nsplit, int32_t* cta_first) {
+  if (check_pairs(pairs, n_pairs) != SERAC_OK || grid <= 0 || grid > MAX_GRID) return SERAC_EINVAL;
+  Plan pl;
+  build_plan(pairs, n_pairs, pl);
+  if (out_chunks) *out_chunks = static_cast<int32_t>(pl.chunks.size());
+  const Chunk& ch = pl.chunks.front();
+  if (out_items) *out_items = static_cast<int32_t>(ch.items);
+  if (out_nsplit)
+    for (int k = ch.p0; k < ch.p1; ++k) out_nsplit[k - ch.p0] = pair_nsplit(pairs[k], ch.nsplit_target);
+  if (cta_first) cut_items(pairs, ch, grid, cta_first);
+  return SERAC_OK;
+}
+
+const char* serac_status_str(int status) {
+  switch (status) {
+    case SERAC_OK: return "ok";
+    case SERAC_EINVAL: return "invalid argument";
+    case SERAC_ECAPACITY: return "match buffer too small (count holds the needed size)";
+    case SERAC_ECUDA: return "CUDA runtime error";
+    case SERAC_ETIMEOUT: return "a bounded wait inside a kernel ran out";
+    case SERAC_EWORKSPACE: return "workspace missing, misaligned or too small";
+    case SERAC_EUNSUPPORTED: return "device is not sm_103 or TMA encoding is unavailable";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

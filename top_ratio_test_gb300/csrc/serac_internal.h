@@ -1,0 +1,101 @@
+// Internal layout shared by the host scheduler (api.cu) and the kernels.
+//
+// Tiling: a pair's score matrix is cut into tiles of BM = 128 rows of A (one
+// tcgen05 accumulator: TMEM lane = row) by BN = 256 rows of B (TMEM columns).
+// Every image is staged once as bf16, zero-padded to a multiple of 256 rows, into
+// one buffer that a single TMA tensor map covers; the zero rows score 0 and the
+// zero floor drops them, so ragged tails need no masking.
+//
+// Work item = (pair, row tile, column split): one A tile resident in shared memory
+// against a contiguous run of B tiles.  Items are cut so that every launch has at
+// least a few items per SM; each CTA of the persistent fused kernel takes a
+// contiguous range of items balanced by tile count.
+#pragma once
+#include <stdint.h>
+
+namespace serac {
+
+constexpr int BM = 128;          // rows of A per tile (MMA M, TMEM lanes)
+constexpr int BN = 256;          // rows of B per tile (MMA N, TMEM columns)
+constexpr int KDIM = 128;        // descriptor length
+constexpr int PAD_ROWS = 256;    // staged images are padded to this many rows
+constexpr int MAX_PAIRS = 128;   // pairs per launch (kernel-parameter tables)
+constexpr int MAX_GRID = 256;    // persistent CTAs per launch
+constexpr int FUSED_THREADS = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+
+__host__ __device__ inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// error bits set by kernels (workspace word 0)
+constexpr int ERR_TIMEOUT_PRODUCER = 1;
+constexpr int ERR_TIMEOUT_MMA = 2;
+constexpr int ERR_TIMEOUT_EPILOGUE = 4;
+
+struct FusedPair {
+  int32_t a_row0;      // first staged row of image A
+  int32_t b_row0;      // first staged row of image B
+  int32_t n_a, n_b;
+  int32_t nsplit;      // column splits per row tile (<= column tiles)
+  int32_t item_base;   // first work item of this pair
+  int64_t colpart_base;  // first column-partial entry of this pair
+};
+
+struct FusedParams {
+  int32_t n_pairs;
+  int32_t n_items;
+  int32_t grid;
+  int32_t dump_ld;                 // score-dump row stride (dump mode only)
+  uint2* colpart;                  // [pair][row tile][n_b padded] (k1, k2)
+  ulonglong2* rowpart;             // [item][half][128] (K1, K2)
+  int32_t* err;                    // error bits
+  int32_t* dump;                   // score dump (dump mode only)
+  int32_t cta_first[MAX_GRID + 1]; // items [cta_first[c], cta_first[c+1]) go to CTA c
+  FusedPair pairs[MAX_PAIRS];
+};
+
+struct StageImage {
+  const uint8_t* src;
+  int32_t n;
+  int32_t row0;  // first staged row
+};
+
+struct StageParams {
+  int32_t n_images;
+  int32_t max_pad_rows;
+  uint16_t* staged;  // bf16 bits, [rows][128]
+  StageImage images[512];
+};
+
+struct FinishPair {
+  int32_t n_a, n_b;
+  int32_t nsplit, item_base;
+  int64_t colpart_base;
+  int32_t row_base;   // first entry of this pair in rowfinal
+  int32_t col_base;   // first entry of this pair in colfinal
+  int32_t* matches;
+  int32_t* count;
+  int32_t* row_top2;
+  int32_t* col_top2;
+  int32_t capacity;
+  int32_t pad_;
+};
+
+struct FinishParams {
+  int32_t n_pairs;
+  int32_t total_rows, total_cols;
+  int32_t ratio_num_sq, ratio_den_sq, norm_sq, min_score, mutual, col_ratio;
+  const uint2* colpart;
+  const ulonglong2* rowpart;
+  int4* rowfinal;
+  int4* colfinal;
+  const int32_t* err;
+  FinishPair pairs[MAX_PAIRS];
+};
+
+// launchers (defined in fused.cu / finish.cu); return a cudaError_t value
+int launch_stage(const StageParams& p, int64_t max_chunks, void* stream);
+int launch_fused(const FusedParams& p, const void* tmap, bool dump, void* stream);
+int launch_reduce(const FinishParams& p, void* stream);
+int launch_match(const FinishParams& p, void* stream);
+int fused_smem_bytes();
+
+}  // namespace serac
