@@ -199,6 +199,8 @@ def run_ours(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     ev_fb = torch.cuda.Event(enable_timing=True)
     ev_fe = torch.cuda.Event(enable_timing=True)
+    ev_fb.record(stream)  # torch creates the CUDA events on first record
+    ev_fe.record(stream)
 
     # one step, captured once
     with torch.cuda.stream(stream):

@@ -107,8 +107,12 @@ def last_launch_count() -> int:
 
 
 def set_profile_events(begin: Optional[torch.cuda.Event], end: Optional[torch.cuda.Event]) -> None:
-    lib().serac_set_profile_events(begin.cuda_event if begin is not None else None,
-                                   end.cuda_event if end is not None else None)
+    """Events must already exist (torch creates them on their first record)."""
+    hb = begin.cuda_event if begin is not None else None
+    he = end.cuda_event if end is not None else None
+    if (begin is not None and not hb) or (end is not None and not he):
+        raise ValueError("record the events once before handing them to the library")
+    lib().serac_set_profile_events(hb, he)
 
 
 def pair_workspace_size(n_a: int, n_b: int) -> int:
