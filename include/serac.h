@@ -143,6 +143,30 @@ int serac_device_check(void);
  * (host-side count, for benchmarking). */
 int serac_last_launch_count(void);
 
+/* Size of the library's built-in scratch used by match_pair_noalloc (16 MiB). */
+#define SERAC_NOALLOC_SCRATCH_BYTES (16 << 20)
+
+/* match_pair without a workspace argument, for callers that may not allocate
+ * device memory: code running inside a host application that owns every device
+ * allocation, real-time loops where an allocation's implicit synchronisation or
+ * failure is not acceptable, tools that must keep a fixed device footprint.  The
+ * paper has no counterpart; it is a deployment convenience.
+ *
+ * Scratch is one fixed array of SERAC_NOALLOC_SCRATCH_BYTES inside the library
+ * (every GPU that loads the library holds it until the process exits).  The call
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ *   - Pairs whose serac_pair_workspace_size(n_a, n_b) exceeds the scratch are
+ *     rejected with SERAC_EWORKSPACE (one 8192 x 8192 pair fits).
+ *   - The first call on each device looks up the scratch's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call before
+ *     any stream capture.
+ *   - All calls share the one scratch array, which keeps the previous call's
+ *     contents (the call clears what must start at zero).  Calls that overlap on the
+ *     GPU (other streams, other host threads) race on it: serialise them.
+ * Arguments, outputs, asynchrony and results are those of match_pair. */
+int match_pair_noalloc(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b, int32_t n_b,
+                       const serac_params* params, const serac_out* out, void* cuda_stream);
+
 /* Host-only view of the work schedule (no GPU needed): for `pairs` (pointers are
  * used only to recognise shared images) and a persistent grid of `grid` CTAs
  * (1..256), report the number of launch chunks, and for the first chunk the number

@@ -19,12 +19,13 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libserac_g
 
 OK, EINVAL, ECAPACITY, ECUDA, ETIMEOUT, EWORKSPACE, EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
 DIM = 128
+NOALLOC_SCRATCH_BYTES = 16 << 20  # SERAC_NOALLOC_SCRATCH_BYTES
 
 # every symbol include/serac.h declares
 EXPORTS = ("serac_default_params", "serac_pair_workspace_size", "match_pair",
            "match_batch_workspace_size", "match_batch", "serac_scores",
            "serac_set_profile_events", "serac_device_check", "serac_last_launch_count",
-           "serac_schedule_describe", "serac_status_str")
+           "serac_schedule_describe", "serac_status_str", "match_pair_noalloc")
 
 
 class SeracError(RuntimeError):
@@ -77,6 +78,7 @@ def lib() -> ctypes.CDLL:
         L.serac_set_profile_events.argtypes = [P, P]
         L.serac_schedule_describe.argtypes = [ctypes.POINTER(_Pair), i32, i32, P, P, P, P]
         L.serac_status_str.restype = ctypes.c_char_p
+        L.match_pair_noalloc.argtypes = [P, i32, P, i32, ctypes.POINTER(Params), ctypes.POINTER(_Out), P]
         _lib_handle = L
     return _lib_handle
 
@@ -180,6 +182,20 @@ def match_pair(a: torch.Tensor, b: torch.Tensor, params: Optional[Params] = None
     st = lib().match_pair(a.data_ptr(), n_a, b.data_ptr(), n_b, ctypes.byref(p), ctypes.byref(c),
                           ws.data_ptr(), ws.numel(), _stream_ptr(stream))
     _check(st, "match_pair")
+    return o
+
+
+def match_pair_noalloc(a: torch.Tensor, b: torch.Tensor, params: Optional[Params] = None, *,
+                       capacity: Optional[int] = None, top2: bool = False, stream=None) -> MatchOutput:
+    """match_pair on the library's built-in scratch, for callers that may not allocate
+    device memory for a workspace (see include/serac.h).  The outputs are still the
+    caller's.  Calls sharing the scratch must not overlap on the GPU."""
+    a, b = _desc(a, "a"), _desc(b, "b")
+    p = params if params is not None else default_params()
+    o, c = _make_out(a.shape[0], b.shape[0], a.device, capacity, top2)
+    st = lib().match_pair_noalloc(a.data_ptr(), a.shape[0], b.data_ptr(), b.shape[0], ctypes.byref(p),
+                                  ctypes.byref(c), _stream_ptr(stream))
+    _check(st, "match_pair_noalloc")
     return o
 
 
