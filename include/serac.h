@@ -156,7 +156,7 @@ int serac_last_launch_count(void);
  * (every GPU that loads the library holds it until the process exits).  The call
  * allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  *   - Pairs whose serac_pair_workspace_size(n_a, n_b) exceeds the scratch are
- *     rejected with SERAC_EWORKSPACE (one 8192 x 8192 pair fits).
+ *     rejected with SERAC_EWORKSPACE (pairs up to 16,384 x 16,384 fit).
  *   - The first call on each device looks up the scratch's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call before
  *     any stream capture.

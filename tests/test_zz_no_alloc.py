@@ -40,8 +40,10 @@ def test_noalloc_matches_match_pair_twice(serac):
 
 
 def test_noalloc_rejects_oversized_pairs(serac):
-    a = torch.zeros((16384, 128), dtype=torch.uint8, device="cuda")
-    assert serac.pair_workspace_size(16384, 16384) > serac.NOALLOC_SCRATCH_BYTES
+    n = 32768
+    assert serac.pair_workspace_size(16384, 16384) <= serac.NOALLOC_SCRATCH_BYTES
+    assert serac.pair_workspace_size(n, n) > serac.NOALLOC_SCRATCH_BYTES
+    a = torch.zeros((n, 128), dtype=torch.uint8, device="cuda")
     with pytest.raises(serac.SeracError) as e:
         serac.match_pair_noalloc(a, a)
     assert e.value.status == serac.EWORKSPACE

@@ -25,7 +25,7 @@ namespace {
 
 constexpr int TARGET_CTAS = 152;            // SMs of a GB300; fixes the item cut
 constexpr int ITEMS_PER_CTA = 8;
-constexpr int64_t CHUNK_COLPART_BYTES = 64ll << 20;
+constexpr int64_t CHUNK_KEY_BYTES = 64ll << 20;
 constexpr size_t ALIGN = 1024;
 
 size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
@@ -34,8 +34,8 @@ struct Chunk {
   int p0 = 0, p1 = 0;          // pairs [p0, p1)
   int nsplit_target = 1;
   int64_t items = 0;
-  int64_t colpart = 0;         // entries
   int64_t rows = 0, cols = 0;  // sum of n_a, n_b
+  int64_t blocks = 0;          // match-kernel blocks
 };
 
 struct Plan {
@@ -43,12 +43,16 @@ struct Plan {
   std::vector<int> a_img, b_img;   // per pair
   int64_t staged_rows = 0;
   std::vector<Chunk> chunks;
-  size_t off_err = 0, off_staged = 0, off_rowpart = 0, off_colpart = 0, off_rowfinal = 0, off_colfinal = 0;
+  size_t off_err = 0, off_staged = 0;
+  // two chunk regions (chunk k uses region k % 2): keys, tickets, look-back status
+  size_t off_region[2] = {0, 0}, region_bytes = 0, r_rowkeys = 0, r_colkeys = 0, r_tickets = 0, r_status = 0;
   size_t total = 0;
 };
 
 int64_t row_tiles(int32_t n_a) { return (static_cast<int64_t>(n_a) + BM - 1) / BM; }
 int64_t col_tiles(int32_t n_b) { return (static_cast<int64_t>(n_b) + BN - 1) / BN; }
+
+int64_t match_blocks(int32_t n_a) { return std::max<int64_t>(1, (static_cast<int64_t>(n_a) + MATCH_ROWS_PER_BLOCK - 1) / MATCH_ROWS_PER_BLOCK); }
 
 int pair_nsplit(const serac_pair& pr, int target) {
   if (pr.n_a <= 0 || pr.n_b <= 0) return 0;
@@ -77,16 +81,17 @@ void build_plan(const serac_pair* pairs, int32_t n_pairs, Plan& pl) {
     pl.a_img[p] = image_of(pairs[p].a, pairs[p].n_a);
     pl.b_img[p] = image_of(pairs[p].b, pairs[p].n_b);
   }
-  // chunks of consecutive pairs
+  // chunks of consecutive pairs, bounded by the kernel-parameter tables and by the
+  // key arrays (16 B per row and per column) they need
   int p = 0;
   while (p < n_pairs || (n_pairs == 0 && pl.chunks.empty())) {
     Chunk ch;
     ch.p0 = p;
-    int64_t colpart = 0;
+    int64_t keys = 0;
     while (p < n_pairs && p - ch.p0 < MAX_PAIRS) {
-      const int64_t cp = row_tiles(pairs[p].n_a) * round_up(pairs[p].n_b, PAD_ROWS);
-      if (p > ch.p0 && (colpart + cp) * 8 > CHUNK_COLPART_BYTES) break;
-      colpart += cp;
+      const int64_t kp = static_cast<int64_t>(pairs[p].n_a) + pairs[p].n_b;
+      if (p > ch.p0 && (keys + kp) * 16 > CHUNK_KEY_BYTES) break;
+      keys += kp;
       ++p;
     }
     ch.p1 = p;
@@ -99,33 +104,37 @@ void build_plan(const serac_pair* pairs, int32_t n_pairs, Plan& pl) {
     for (int k = ch.p0; k < ch.p1; ++k) {
       const int ns = pair_nsplit(pairs[k], ch.nsplit_target);
       ch.items += row_tiles(pairs[k].n_a) * ns;
-      if (ns > 0) ch.colpart += row_tiles(pairs[k].n_a) * round_up(pairs[k].n_b, PAD_ROWS);
       ch.rows += pairs[k].n_a;
       ch.cols += pairs[k].n_b;
+      ch.blocks += match_blocks(pairs[k].n_a);
     }
     pl.chunks.push_back(ch);
     if (n_pairs == 0) break;
   }
-  int64_t max_items = 0, max_colpart = 0, max_rows = 0, max_cols = 0;
+  int64_t max_rows = 0, max_cols = 0, max_blocks = 0;
   for (const Chunk& ch : pl.chunks) {
-    max_items = std::max(max_items, ch.items);
-    max_colpart = std::max(max_colpart, ch.colpart);
     max_rows = std::max(max_rows, ch.rows);
     max_cols = std::max(max_cols, ch.cols);
+    max_blocks = std::max(max_blocks, ch.blocks);
   }
   size_t off = 0;
   pl.off_err = off;
   off = align_up(off + 256);
   pl.off_staged = off;
   off = align_up(off + static_cast<size_t>(pl.staged_rows) * KDIM * 2);
-  pl.off_rowpart = off;
-  off = align_up(off + static_cast<size_t>(max_items) * 2 * BM * sizeof(ulonglong2));
-  pl.off_colpart = off;
-  off = align_up(off + static_cast<size_t>(max_colpart) * sizeof(uint2));
-  pl.off_rowfinal = off;
-  off = align_up(off + static_cast<size_t>(max_rows) * sizeof(int4));
-  pl.off_colfinal = off;
-  off = align_up(off + static_cast<size_t>(max_cols) * sizeof(int4));
+  size_t r = 0;
+  pl.r_rowkeys = r;
+  r = align_up(r + static_cast<size_t>(max_rows) * 16);
+  pl.r_colkeys = r;
+  r = align_up(r + static_cast<size_t>(max_cols) * 16);
+  pl.r_tickets = r;
+  r = align_up(r + static_cast<size_t>(MAX_PAIRS) * 4);
+  pl.r_status = r;
+  r = align_up(r + static_cast<size_t>(max_blocks) * 8);
+  pl.region_bytes = r;
+  pl.off_region[0] = off;
+  pl.off_region[1] = pl.chunks.size() > 1 ? off + r : off;  // one chunk needs one region
+  off += pl.chunks.size() > 1 ? 2 * r : r;
   pl.total = off;
 }
 
@@ -276,53 +285,67 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
     st = encode_staged_map(&map, staged, pl.staged_rows);
     if (st != SERAC_OK) return st;
   }
-  SERAC_TRY_CUDA(cudaMemsetAsync(err, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)));
 
-  // staging, 512 images per launch
-  for (size_t i0 = 0; i0 < pl.images.size(); i0 += 512) {
+  // staging (512 images per launch); the first launch also clears the error word and
+  // the key arrays, which every match launch leaves cleared behind it
+  for (size_t i0 = 0; i0 == 0 || i0 < pl.images.size(); i0 += 512) {
     StageParams sp;
-    sp.n_images = 0;
-    sp.max_pad_rows = 0;
+    std::memset(&sp, 0, sizeof(sp));
     sp.staged = staged;
+    sp.err = err;
+    if (i0 == 0) {
+      sp.zero = reinterpret_cast<uint4*>(ws + pl.off_region[0]);
+      sp.zero_n = static_cast<int64_t>((pl.total - pl.off_region[0]) / 16);
+      sp.zero_blocks = static_cast<int32_t>(std::min<int64_t>(1024, (sp.zero_n + 255) / 256));
+      if (sp.zero_blocks < 1) sp.zero_blocks = 1;
+    }
     int64_t max_chunks = 0;
     for (size_t i = i0; i < pl.images.size() && i < i0 + 512; ++i) {
       if (pl.images[i].n == 0) continue;
       sp.images[sp.n_images++] = pl.images[i];
       max_chunks = std::max<int64_t>(max_chunks, round_up(pl.images[i].n, PAD_ROWS) * (KDIM / 16));
     }
-    if (sp.n_images == 0) continue;
+    if (sp.n_images == 0 && i0 > 0) continue;
     if (launch_stage(sp, max_chunks, stream) != 0) return SERAC_ECUDA;
     ++g_last_launches;
   }
 
   bool first_fused = true;
-  for (const Chunk& ch : pl.chunks) {
-    // ---------------- fused GEMM + top-2
+  for (size_t ci = 0; ci < pl.chunks.size(); ++ci) {
+    const Chunk& ch = pl.chunks[ci];
+    uint8_t* region = ws + pl.off_region[ci & 1];
+    uint8_t* other = ws + pl.off_region[(ci + 1) & 1];
+    unsigned long long* rowkeys = reinterpret_cast<unsigned long long*>(region + pl.r_rowkeys);
+    unsigned long long* colkeys = reinterpret_cast<unsigned long long*>(region + pl.r_colkeys);
+    // ---------------- fused GEMM + top-2, merged into the key arrays
     if (ch.items > 0) {
       FusedParams fp;
       std::memset(&fp, 0, sizeof(fp));
       fp.grid = static_cast<int32_t>(std::min<int64_t>({static_cast<int64_t>(sms), ch.items, MAX_GRID}));
       fp.n_items = static_cast<int32_t>(ch.items);
-      fp.colpart = reinterpret_cast<uint2*>(ws + pl.off_colpart);
-      fp.rowpart = reinterpret_cast<ulonglong2*>(ws + pl.off_rowpart);
+      fp.rowkeys = rowkeys;
+      fp.colkeys = colkeys;
       fp.err = err;
       fp.dump = dump;
       fp.dump_ld = (dump && n_pairs > 0) ? pairs[0].n_b : 0;
       int np = 0;
-      int64_t item_base = 0, colpart_base = 0;
+      int64_t item_base = 0, rows = 0, cols = 0;
       for (int k = ch.p0; k < ch.p1; ++k) {
         const int ns = pair_nsplit(pairs[k], ch.nsplit_target);
-        if (ns == 0) continue;
-        FusedPair& f = fp.pairs[np++];
-        f.a_row0 = pl.images[pl.a_img[k]].row0;
-        f.b_row0 = pl.images[pl.b_img[k]].row0;
-        f.n_a = pairs[k].n_a;
-        f.n_b = pairs[k].n_b;
-        f.nsplit = ns;
-        f.item_base = static_cast<int32_t>(item_base);
-        f.colpart_base = colpart_base;
-        item_base += row_tiles(pairs[k].n_a) * ns;
-        colpart_base += row_tiles(pairs[k].n_a) * round_up(pairs[k].n_b, PAD_ROWS);
+        if (ns > 0) {
+          FusedPair& f = fp.pairs[np++];
+          f.a_row0 = pl.images[pl.a_img[k]].row0;
+          f.b_row0 = pl.images[pl.b_img[k]].row0;
+          f.n_a = pairs[k].n_a;
+          f.n_b = pairs[k].n_b;
+          f.nsplit = ns;
+          f.item_base = static_cast<int32_t>(item_base);
+          f.row_base = static_cast<int32_t>(rows);
+          f.col_base = static_cast<int32_t>(cols);
+          item_base += row_tiles(pairs[k].n_a) * ns;
+        }
+        rows += pairs[k].n_a;
+        cols += pairs[k].n_b;
       }
       fp.n_pairs = np;
       cut_items(pairs, ch, fp.grid, fp.cta_first);
@@ -336,7 +359,7 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
       first_fused = false;
     }
     if (dump) continue;
-    // ---------------- reduce + match
+    // ---------------- decisions and compaction (clears the keys it read)
     FinishParams fn;
     std::memset(&fn, 0, sizeof(fn));
     fn.ratio_num_sq = params->ratio_num_sq;
@@ -345,21 +368,21 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
     fn.min_score = params->min_score;
     fn.mutual = params->mutual;
     fn.col_ratio = params->col_ratio;
-    fn.colpart = reinterpret_cast<const uint2*>(ws + pl.off_colpart);
-    fn.rowpart = reinterpret_cast<const ulonglong2*>(ws + pl.off_rowpart);
-    fn.rowfinal = reinterpret_cast<int4*>(ws + pl.off_rowfinal);
-    fn.colfinal = reinterpret_cast<int4*>(ws + pl.off_colfinal);
+    fn.rowkeys = rowkeys;
+    fn.colkeys = colkeys;
+    fn.tickets = reinterpret_cast<int32_t*>(region + pl.r_tickets);
+    fn.status = reinterpret_cast<unsigned long long*>(region + pl.r_status);
+    // the next chunk's region was last used by the previous chunk, whose match
+    // launch has finished before this chunk's fused launch began
+    fn.zero = pl.chunks.size() > 1 ? reinterpret_cast<uint4*>(other) : nullptr;
+    fn.zero_n = pl.chunks.size() > 1 ? static_cast<int64_t>(pl.region_bytes / 16) : 0;
     fn.err = err;
-    int64_t item_base = 0, colpart_base = 0, rows = 0, cols = 0;
+    int64_t rows = 0, cols = 0, blocks = 0;
     int np = 0;
     for (int k = ch.p0; k < ch.p1; ++k) {
-      const int ns = pair_nsplit(pairs[k], ch.nsplit_target);
       FinishPair& f = fn.pairs[np++];
       f.n_a = pairs[k].n_a;
       f.n_b = pairs[k].n_b;
-      f.nsplit = ns;
-      f.item_base = static_cast<int32_t>(item_base);
-      f.colpart_base = colpart_base;
       f.row_base = static_cast<int32_t>(rows);
       f.col_base = static_cast<int32_t>(cols);
       f.matches = outs[k].matches;
@@ -367,20 +390,14 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
       f.row_top2 = outs[k].row_top2;
       f.col_top2 = outs[k].col_top2;
       f.capacity = outs[k].capacity;
-      if (ns > 0) {
-        item_base += row_tiles(pairs[k].n_a) * ns;
-        colpart_base += row_tiles(pairs[k].n_a) * round_up(pairs[k].n_b, PAD_ROWS);
-      }
+      f.blk_base = static_cast<int32_t>(blocks);
+      f.nblk = static_cast<int32_t>(match_blocks(pairs[k].n_a));
+      blocks += f.nblk;
       rows += pairs[k].n_a;
       cols += pairs[k].n_b;
     }
     fn.n_pairs = np;
-    fn.total_rows = static_cast<int32_t>(rows);
-    fn.total_cols = static_cast<int32_t>(cols);
-    if (rows + cols > 0) {
-      if (launch_reduce(fn, stream) != 0) return SERAC_ECUDA;
-      ++g_last_launches;
-    }
+    fn.total_blocks = static_cast<int32_t>(blocks);
     if (np > 0) {
       if (launch_match(fn, stream) != 0) return SERAC_ECUDA;
       ++g_last_launches;

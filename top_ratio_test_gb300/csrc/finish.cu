@@ -1,14 +1,14 @@
-// Operand staging, partial reduction and the match decision with compaction.
+// Operand staging and the match decision with compaction.
 //
 //   stage:  u8 descriptors -> bf16 rows of the staged buffer, each image zero-padded
-//           to a multiple of 256 rows (bytes 0..255 are exact in bf16).
-//   reduce: per row, fold the row partials of its column splits; per column, fold
-//           the per-row-tile column partials ("Wider tiles" on the "SERAC" page: the
-//           column-partial table that ColMatch consumes) into the final top-2 with
-//           global indices, ties to the lower index.
-//   match:  per pair, one block tests every row, looks up its best column, applies
-//           the mutual check and the column test, and writes the kept (i, j) in
-//           ascending i with a warp-ballot / block-scan compaction.
+//           to a multiple of 256 rows (bytes 0..255 are exact in bf16); an extra row
+//           of blocks clears the key arrays the fused kernel merges into.
+//   match:  per pair, blocks of 512 rows decode every row's top-2 key, test it, look
+//           up its best column's top-2, apply the mutual check and the column test
+//           ("SERAC", "Exactness": ratio test, cross check), and write the kept (i, j)
+//           in ascending i: a block-wide scan of per-thread counts, then a decoupled
+//           look-back over the pair's earlier blocks for the block's offset.  Each
+//           launch also clears the other launch chunk's key region.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -21,6 +21,15 @@ namespace serac {
 namespace {
 
 __global__ void __launch_bounds__(256) stage_kernel(const __grid_constant__ StageParams P) {
+  if (blockIdx.y == static_cast<unsigned>(P.n_images)) {
+    // clear the key arrays and the error word
+    if (blockIdx.x >= static_cast<unsigned>(P.zero_blocks)) return;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *P.err = 0;
+    for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < P.zero_n;
+         c += static_cast<int64_t>(P.zero_blocks) * blockDim.x)
+      P.zero[c] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
   const StageImage im = P.images[blockIdx.y];
   const int64_t n_pad = round_up(im.n, PAD_ROWS);
   const int64_t chunks = n_pad * (KDIM / 16);  // 16-byte input chunks
@@ -46,78 +55,14 @@ __global__ void __launch_bounds__(256) stage_kernel(const __grid_constant__ Stag
   }
 }
 
-__device__ __forceinline__ void ins2_64(uint64_t& k1, uint64_t& k2, uint64_t x) {
-  if (x > k1) { k2 = k1; k1 = x; } else if (x > k2) { k2 = x; }
-}
-
-// 64-bit key (s << 32 | 0xFFFFFFFF - index), 0 = empty -> (s1, i1, s2, i2)
-__device__ __forceinline__ int4 decode2(uint64_t k1, uint64_t k2) {
+// (best, second) 64-bit keys (s << 32 | 0xFFFFFFFF - index, 0 = empty) -> (s1, i1, s2, i2)
+__device__ __forceinline__ int4 decode2(unsigned long long k1, unsigned long long k2) {
   int4 r;
   r.x = static_cast<int>(k1 >> 32);
   r.y = k1 ? static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k1)) : -1;
   r.z = static_cast<int>(k2 >> 32);
   r.w = k2 ? static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k2)) : -1;
   return r;
-}
-
-template <typename F>
-__device__ __forceinline__ int find_pair(const FinishParams& P, int64_t t, F base_of) {
-  int lo = 0, hi = P.n_pairs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (base_of(P.pairs[mid]) <= t) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
-__global__ void __launch_bounds__(256) reduce_kernel(const __grid_constant__ FinishParams P) {
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t < P.total_rows) {
-    const int p = find_pair(P, t, [](const FinishPair& f) { return static_cast<int64_t>(f.row_base); });
-    const FinishPair& fp = P.pairs[p];
-    const int i = static_cast<int>(t - fp.row_base);
-    uint64_t k1 = 0, k2 = 0;
-    if (fp.nsplit > 0) {
-      const int rt = i / BM, rl = i - rt * BM;
-      for (int s = 0; s < fp.nsplit; ++s) {
-        const int64_t item = static_cast<int64_t>(fp.item_base) + static_cast<int64_t>(rt) * fp.nsplit + s;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const ulonglong2 x = P.rowpart[(item * 2 + h) * BM + rl];
-          ins2_64(k1, k2, x.x);
-          ins2_64(k1, k2, x.y);
-        }
-      }
-    }
-    const int4 r = decode2(k1, k2);
-    P.rowfinal[t] = r;
-    if (fp.row_top2) reinterpret_cast<int4*>(fp.row_top2)[i] = r;
-  } else if (t < static_cast<int64_t>(P.total_rows) + P.total_cols) {
-    const int64_t tc = t - P.total_rows;
-    const int p = find_pair(P, tc, [](const FinishPair& f) { return static_cast<int64_t>(f.col_base); });
-    const FinishPair& fp = P.pairs[p];
-    const int j = static_cast<int>(tc - fp.col_base);
-    uint64_t k1 = 0, k2 = 0;
-    if (fp.nsplit > 0) {
-      const int rts = (fp.n_a + BM - 1) / BM;
-      const int64_t nb_pad = round_up(fp.n_b, PAD_ROWS);
-      for (int rt = 0; rt < rts; ++rt) {
-        const uint2 x = P.colpart[fp.colpart_base + rt * nb_pad + j];
-        const uint32_t kk[2] = {x.x, x.y};
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const uint32_t s = kk[u] >> 8;
-          if (s) {
-            const uint32_t i = static_cast<uint32_t>(rt * BM) + (127u - (kk[u] & 255u));
-            ins2_64(k1, k2, (static_cast<uint64_t>(s) << 32) | (0xFFFFFFFFu - i));
-          }
-        }
-      }
-    }
-    const int4 r = decode2(k1, k2);
-    P.colfinal[tc] = r;
-    if (fp.col_top2) reinterpret_cast<int4*>(fp.col_top2)[j] = r;
-  }
 }
 
 __device__ __forceinline__ bool passes(const FinishParams& P, const int4& t) {
@@ -127,73 +72,149 @@ __device__ __forceinline__ bool passes(const FinishParams& P, const int4& t) {
   return lhs < rhs && t.x >= P.min_score;
 }
 
-constexpr int MATCH_THREADS = 1024;
+constexpr unsigned long long LB_AGG = 1ull << 32;   // status word: block aggregate published
+constexpr unsigned long long LB_INCL = 2ull << 32;  // status word: inclusive prefix published
+constexpr uint64_t LB_LIMIT_NS = 1000000000ull;
+
+__device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __global__ void __launch_bounds__(MATCH_THREADS) match_kernel(const __grid_constant__ FinishParams P) {
-  const FinishPair& fp = P.pairs[blockIdx.x];
-  __shared__ int warp_off[32];
-  __shared__ int block_total;
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int base = 0;
-  for (int i0 = 0; i0 < fp.n_a; i0 += MATCH_THREADS) {
-    const int i = i0 + static_cast<int>(threadIdx.x);
-    int j = -1;
-    if (i < fp.n_a) {
-      const int4 r = P.rowfinal[fp.row_base + i];
-      if (passes(P, r)) {
-        const int4 c = P.colfinal[fp.col_base + r.y];
-        if ((!P.mutual || c.y == i) && (!P.col_ratio || passes(P, c))) j = r.y;
-      }
-    }
-    const unsigned m = __ballot_sync(0xffffffffu, j >= 0);
-    if (lane == 0) warp_off[w] = __popc(m);
-    __syncthreads();
-    if (w == 0) {
-      const int v = warp_off[lane];
-      int incl = v;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d) incl += y;
-      }
-      warp_off[lane] = incl - v;
-      if (lane == 31) block_total = incl;
-    }
-    __syncthreads();
-    if (j >= 0) {
-      const int pos = base + warp_off[w] + __popc(m & ((1u << lane) - 1u));
-      if (pos < fp.capacity) {
-        fp.matches[2 * static_cast<int64_t>(pos)] = i;
-        fp.matches[2 * static_cast<int64_t>(pos) + 1] = j;
-      }
-    }
-    base += block_total;
-    __syncthreads();
+  // this block's pair
+  int lo = 0, hi = P.n_pairs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.pairs[mid].blk_base <= static_cast<int>(blockIdx.x)) lo = mid; else hi = mid - 1;
   }
-  if (threadIdx.x == 0) *fp.count = (*P.err != 0) ? SERAC_ETIMEOUT : base;
+  const FinishPair& fp = P.pairs[lo];
+  const ulonglong2* rk = reinterpret_cast<const ulonglong2*>(P.rowkeys) + fp.row_base;
+  const ulonglong2* ck = reinterpret_cast<const ulonglong2*>(P.colkeys) + fp.col_base;
+  __shared__ int s_b, s_prefix;
+  __shared__ int warp_off[MATCH_THREADS / 32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  // block order within the pair by ticket: a block only ever waits on blocks that
+  // have already started
+  if (threadIdx.x == 0) s_b = atomicAdd(&P.tickets[lo], 1);
+  __syncthreads();
+  const int b = s_b;
+
+  const int ib = b * MATCH_ROWS_PER_BLOCK + static_cast<int>(threadIdx.x) * MATCH_ROWS_PER_THREAD;
+  int4 rt[MATCH_ROWS_PER_THREAD];
+#pragma unroll
+  for (int k = 0; k < MATCH_ROWS_PER_THREAD; ++k) {
+    const ulonglong2 x = (ib + k < fp.n_a) ? rk[ib + k] : make_ulonglong2(0ull, 0ull);
+    rt[k] = decode2(x.x, x.y);
+    if (fp.row_top2 && ib + k < fp.n_a) reinterpret_cast<int4*>(fp.row_top2)[ib + k] = rt[k];
+  }
+  ulonglong2 cx[MATCH_ROWS_PER_THREAD];
+#pragma unroll
+  for (int k = 0; k < MATCH_ROWS_PER_THREAD; ++k)
+    cx[k] = passes(P, rt[k]) ? ck[rt[k].y] : make_ulonglong2(0ull, 0ull);
+  int cnt = 0;
+  uint32_t keep = 0;
+#pragma unroll
+  for (int k = 0; k < MATCH_ROWS_PER_THREAD; ++k) {
+    if (!passes(P, rt[k])) continue;
+    const int4 c = decode2(cx[k].x, cx[k].y);
+    if ((!P.mutual || c.y == ib + k) && (!P.col_ratio || passes(P, c))) {
+      keep |= 1u << k;
+      ++cnt;
+    }
+  }
+  // exclusive scan of per-thread counts over the block (thread order = row order)
+  int incl = cnt;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  if (lane == 31) warp_off[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    constexpr int NW = MATCH_THREADS / 32;
+    const int v = lane < NW ? warp_off[lane] : 0;
+    int s = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, d);
+      if (lane >= d) s += y;
+    }
+    if (lane < NW) warp_off[lane] = s - v;
+    if (lane == 31) {
+      // decoupled look-back over the pair's earlier blocks
+      const int total = s;
+      unsigned long long* st = P.status + fp.blk_base;
+      int prefix = 0;
+      if (b == 0) {
+        atomicExch(&st[0], LB_INCL | static_cast<uint32_t>(total));
+      } else {
+        atomicExch(&st[b], LB_AGG | static_cast<uint32_t>(total));
+        const uint64_t t0 = now_ns();
+        for (int k = b - 1; k >= 0;) {
+          const unsigned long long wv = *reinterpret_cast<volatile unsigned long long*>(&st[k]);
+          if (wv == 0ull) {
+            if (now_ns() - t0 > LB_LIMIT_NS) {
+              atomicOr(P.err, ERR_TIMEOUT_LOOKBACK);
+              break;
+            }
+            continue;
+          }
+          prefix += static_cast<int>(static_cast<uint32_t>(wv));
+          if ((wv & ~0xFFFFFFFFull) == LB_INCL) break;
+          --k;
+        }
+        atomicExch(&st[b], LB_INCL | static_cast<uint32_t>(prefix + total));
+      }
+      s_prefix = prefix;
+      if (b == fp.nblk - 1) *fp.count = (*reinterpret_cast<volatile int32_t*>(P.err) != 0) ? SERAC_ETIMEOUT : prefix + total;
+    }
+  }
+  __syncthreads();
+  int pos = s_prefix + warp_off[w] + incl - cnt;
+#pragma unroll
+  for (int k = 0; k < MATCH_ROWS_PER_THREAD; ++k) {
+    if (keep & (1u << k)) {
+      if (pos < fp.capacity) {
+        fp.matches[2 * static_cast<int64_t>(pos)] = ib + k;
+        fp.matches[2 * static_cast<int64_t>(pos) + 1] = rt[k].y;
+      }
+      ++pos;
+    }
+  }
+  // optional column top-2, split over the pair's blocks
+  if (fp.col_top2) {
+    const int per = (fp.n_b + fp.nblk - 1) / fp.nblk;
+    const int j1 = min(fp.n_b, (b + 1) * per);
+    for (int j = b * per + static_cast<int>(threadIdx.x); j < j1; j += MATCH_THREADS) {
+      const ulonglong2 x = ck[j];
+      reinterpret_cast<int4*>(fp.col_top2)[j] = decode2(x.x, x.y);
+    }
+  }
+  // clear the other chunk's key region, split over the whole launch
+  const int64_t per = (P.zero_n + P.total_blocks - 1) / P.total_blocks;
+  const int64_t z1 = min(P.zero_n, (static_cast<int64_t>(blockIdx.x) + 1) * per);
+  for (int64_t z = static_cast<int64_t>(blockIdx.x) * per + threadIdx.x; z < z1; z += MATCH_THREADS)
+    P.zero[z] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 }  // namespace
 
 int launch_stage(const StageParams& p, int64_t max_chunks, void* stream) {
-  if (p.n_images == 0) return 0;
   int64_t blocks = (max_chunks + 255) / 256;
   if (blocks > 1024) blocks = 1024;
+  if (blocks < p.zero_blocks) blocks = p.zero_blocks;
   if (blocks < 1) blocks = 1;
-  stage_kernel<<<dim3(static_cast<unsigned>(blocks), p.n_images), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
-  return static_cast<int>(cudaGetLastError());
-}
-
-int launch_reduce(const FinishParams& p, void* stream) {
-  const int64_t n = static_cast<int64_t>(p.total_rows) + p.total_cols;
-  if (n == 0) return 0;
-  reduce_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+  stage_kernel<<<dim3(static_cast<unsigned>(blocks), p.n_images + 1), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      p);
   return static_cast<int>(cudaGetLastError());
 }
 
 int launch_match(const FinishParams& p, void* stream) {
-  if (p.n_pairs == 0) return 0;
-  match_kernel<<<p.n_pairs, MATCH_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(p);
+  if (p.total_blocks == 0) return 0;
+  match_kernel<<<p.total_blocks, MATCH_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(p);
   return static_cast<int>(cudaGetLastError());
 }
 

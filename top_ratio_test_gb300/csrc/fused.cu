@@ -2,30 +2,40 @@
 //
 // The "SERAC" page ("What changed": DP4A, fused row reduction, wider tiles) keeps
 // the best two scores of each row in registers while the dot products are formed,
-// so the num1 x num2 matrix is never written, and emits per-block column partials
-// for the cross check.  This kernel keeps that dataflow but forms the dot products
-// on the sm_103a tensor cores instead of DP4A:
+// so the num1 x num2 matrix is never written, and reduces the column direction from
+// per-block partials for the cross check.  This kernel keeps that dataflow but forms
+// the dot products on the sm_103a tensor cores instead of DP4A:
 //
-//   * a persistent CTA per SM walks a contiguous range of work items; an item is one
-//     128-row tile of A (resident in shared memory) against a run of 256-row tiles of
-//     B streamed by TMA (128-byte swizzle, two stages);
+//   * a persistent CTA per SM walks a contiguous range of work items; consecutive
+//     items on the same row tile form a segment: one 128-row tile of A resident in
+//     shared memory against a run of 256-row tiles of B streamed by TMA (128-byte
+//     swizzle, two stages);
 //   * one thread issues tcgen05.mma kind::f16 (bf16 x bf16 -> f32, M=128, N=256,
 //     K=16 x 8) into one of two TMEM accumulators (2 x 256 columns), so the epilogue
 //     of tile t overlaps the MMAs of tile t+1.  u8 values are exact in bf16 and every
 //     partial sum is an integer below 2^24, so the f32 accumulator holds the exact
 //     integer score ("Exactness": 128 * 255^2 = 8,323,200 cannot overflow);
-//   * eight epilogue warps read the accumulator (thread = row, 128 columns each) and
+//   * sixteen epilogue warps (four per SM sub-partition) read the accumulator
+//     (thread = row, 64 columns each) and
 //       - add 2^23, which turns the f32 score s into the integer bits 0x4B000000 | s,
-//       - build packed keys (s << 8 | 255 - column) for the row and
-//         (s << 8 | 127 - row) for the column, so a plain unsigned max orders by score
-//         then lower index -- the order-independent tie rule of "Real-Time Dense
-//         Stereo at 34 Hz on a Jetson TX2 (MASDA, Part 3)", section 6, which packs
-//         (value, k) into one integer for its fused warp top-2,
-//       - keep the row top-2 in registers across the item's tiles,
-//       - transpose each 32 x 32 block of column keys through shared memory, take the
-//         top-2 of every column over the warp's 32 rows, then merge the four row
-//         quadrants into one (k1, k2) per column per row tile: the column partials a
-//         second kernel reduces ("Wider tiles": the column-partial table).
+//       - build packed keys s << 8 | index with one integer multiply-add each (the
+//         multiply by 256 shifts the exponent bits out), so a plain max orders by
+//         score then lower index -- the order-independent tie rule of "Real-Time
+//         Dense Stereo at 34 Hz on a Jetson TX2 (MASDA, Part 3)", section 6, which
+//         packs (value, k) into one integer for its fused warp top-2.  Every key is
+//         below 0x7F800000, so keys also compare correctly as finite floats and the
+//         3-input float max can merge them;
+//       - reduce each 32-key chunk with a tree (for instruction-level parallelism)
+//         and keep the row top-2 in registers across the segment,
+//       - transpose column keys through shared memory in 16-column half-blocks,
+//         take the top-2 of every column over the warp's 32 rows (two lanes per
+//         column, one shuffle), merge the four row quadrants,
+//         and fold the tile's column top-2 into the column's global top-2 with 64-bit
+//         atomicMax ("Wider tiles": the column partials, here merged in place).
+//
+// Global top-2 by atomics: old = max(best, x1); second = max(second, min(old, x1));
+// second = max(second, x2).  Every candidate other than the final best reaches
+// `second`, the final best never does (keys are unique), whatever the order.
 //
 // Zero-padded rows and columns score 0 and fall to the zero floor, so ragged tails
 // need no masking.  Every wait is bounded; a timeout sets an error bit that the
@@ -47,9 +57,9 @@ constexpr int A_HALF = BM * 64 * 2;      // 16 KB: 128 rows x 64 bf16 (128 B)
 constexpr int B_BYTES = BN * KDIM * 2;   // 64 KB
 constexpr int B_HALF = BN * 64 * 2;      // 32 KB
 constexpr int BOX_BYTES = 128 * 64 * 2;  // 16 KB: one TMA box (64 x 128)
-constexpr int NUM_EPI_WARPS = 8;
-constexpr int T_STRIDE = 36;             // transpose block: 32 columns x 36 words (padded)
-constexpr int T_WARP_WORDS = 32 * T_STRIDE;
+constexpr int NUM_EPI_WARPS = 16;
+constexpr int T_STRIDE = 36;             // transpose half-block: 16 columns x 36 words (padded)
+constexpr int T_WARP_WORDS = 16 * T_STRIDE;
 
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + A_BYTES;
@@ -82,22 +92,74 @@ __device__ __forceinline__ Item decode_item(const FusedParams& P, int item) {
   return Item{lo, rt, s * ct_total / fp.nsplit, (s + 1) * ct_total / fp.nsplit};
 }
 
-// Insert a key into a top-2 of distinct keys (k1 > k2).
-__device__ __forceinline__ void ins2(uint32_t& k1, uint32_t& k2, uint32_t x) {
-  const uint32_t t = min(k1, x);
-  k1 = max(k1, x);
-  k2 = max(k2, t);
-}
-__device__ __forceinline__ void ins2_64(uint64_t& k1, uint64_t& k2, uint64_t x) {
-  if (x > k1) { k2 = k1; k1 = x; } else if (x > k2) { k2 = x; }
+// The segment starting at item `it`: the run of items [it, next) on one row tile.
+struct Segment {
+  Item s;
+  int next;
+};
+
+__device__ __forceinline__ Segment next_segment(const FusedParams& P, int it, int it1) {
+  Segment g{decode_item(P, it), it + 1};
+  while (g.next < it1) {
+    const Item J = decode_item(P, g.next);
+    if (J.p != g.s.p || J.rt != g.s.rt) break;
+    g.s.ct1 = J.ct1;
+    ++g.next;
+  }
+  return g;
 }
 
-// Tile-local row key (s << 8 | 255 - column) -> 64-bit (s << 32 | ~j); 0 if s == 0.
-__device__ __forceinline__ uint64_t row_key64(uint32_t k, int col0) {
+// ---- key arithmetic
+__device__ __forceinline__ uint32_t mad_lo(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Merge top-2 (b1, b2) into top-2 (a1, a2).
+__device__ __forceinline__ void merge2(float& a1, float& a2, float b1, float b2) {
+  const float m = fminf(a1, b1);
+  a1 = fmaxf(a1, b1);
+  a2 = fmax3(a2, m, b2);
+}
+// Top-2 of N distinct keys as a tree (pairwise, then pairwise merges): the same
+// number of min/max as a sequential scan, but log2(N) deep instead of N.
+template <int N>
+__device__ __forceinline__ void tree_top2(const float (&x)[N], float& k1, float& k2) {
+  float hi[N / 2], lo[N / 2];
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    hi[i] = fmaxf(x[2 * i], x[2 * i + 1]);
+    lo[i] = fminf(x[2 * i], x[2 * i + 1]);
+  }
+#pragma unroll
+  for (int w = N / 4; w >= 1; w >>= 1) {
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      float a1 = hi[2 * i], a2 = lo[2 * i];
+      merge2(a1, a2, hi[2 * i + 1], lo[2 * i + 1]);
+      hi[i] = a1;
+      lo[i] = a2;
+    }
+  }
+  k1 = hi[0];
+  k2 = lo[0];
+}
+__device__ __forceinline__ void ins2_64(unsigned long long& k1, unsigned long long& k2, unsigned long long x) {
+  if (x > k2) {
+    if (x > k1) { k2 = k1; k1 = x; } else { k2 = x; }
+  }
+}
+// 32-bit key s << 8 | (255 - local) -> 64-bit s << 32 | ~(base + local); 0 if s == 0.
+__device__ __forceinline__ unsigned long long key64(uint32_t k, uint32_t base) {
   const uint32_t s = k >> 8;
-  if (s == 0) return 0;
-  const uint32_t j = static_cast<uint32_t>(col0) + (255u - (k & 255u));
-  return (static_cast<uint64_t>(s) << 32) | (0xFFFFFFFFu - j);
+  if (s == 0) return 0ull;
+  const uint32_t idx = base + (255u - (k & 255u));
+  return (static_cast<unsigned long long>(s) << 32) | (0xFFFFFFFFu - idx);
 }
 
 // Bounded wait by lane 0, result broadcast to the warp.
@@ -122,10 +184,10 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
   uint64_t* b_empty = bars + 4;   // [2]
   uint64_t* t_full = bars + 6;    // [2]
   uint64_t* t_empty = bars + 8;   // [2]
-  uint64_t* merged = bars + 10;   // [parity 2][half 2]
-  uint64_t* drain = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
+  uint64_t* merged = bars + 10;   // [parity 2][quarter 4]
+  uint64_t* drain = bars + 18;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 20);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -138,7 +200,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
       mbar_init(&t_full[i], 1);
       mbar_init(&t_empty[i], NUM_EPI_WARPS);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&merged[i], 4);
+    for (int i = 0; i < 8; ++i) mbar_init(&merged[i], 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -158,18 +220,18 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      uint32_t bcount = 0;
-      for (int it = it0; it < it1; ++it) {
-        const Item I = decode_item(P, it);
-        const FusedPair& fp = P.pairs[I.p];
-        const uint32_t n_local = static_cast<uint32_t>(it - it0);
-        if (!mbar_wait(a_empty, (n_local & 1u) ^ 1u, abort_flag, P.err, ERR_TIMEOUT_PRODUCER, WAIT_LIMIT_NS)) break;
+      uint32_t bcount = 0, nseg = 0;
+      bool ok = true;
+      for (int it = it0; it < it1 && ok; ++nseg) {
+        const Segment g = next_segment(P, it, it1);
+        it = g.next;
+        const FusedPair& fp = P.pairs[g.s.p];
+        if (!mbar_wait(a_empty, (nseg & 1u) ^ 1u, abort_flag, P.err, ERR_TIMEOUT_PRODUCER, WAIT_LIMIT_NS)) break;
         mbar_arrive_expect_tx(a_full, A_BYTES);
-        const int ay = fp.a_row0 + I.rt * BM;
+        const int ay = fp.a_row0 + g.s.rt * BM;
         tma_load_2d(sA, &tmap, a_full, 0, ay);
         tma_load_2d(sA + A_HALF, &tmap, a_full, 64, ay);
-        bool ok = true;
-        for (int ct = I.ct0; ct < I.ct1; ++ct, ++bcount) {
+        for (int ct = g.s.ct0; ct < g.s.ct1; ++ct, ++bcount) {
           const uint32_t st = bcount & 1u, ph = (bcount >> 1) & 1u;
           if (!mbar_wait(&b_empty[st], ph ^ 1u, abort_flag, P.err, ERR_TIMEOUT_PRODUCER, WAIT_LIMIT_NS)) {
             ok = false;
@@ -183,7 +245,6 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
           tma_load_2d(dst + B_HALF, &tmap, &b_full[st], 64, by);
           tma_load_2d(dst + B_HALF + BOX_BYTES, &tmap, &b_full[st], 64, by + 128);
         }
-        if (!ok) break;
       }
       if (*abort_flag) {
         // let any copy still in flight land before shared memory is released
@@ -195,15 +256,15 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t bcount = 0, tcount = 0;
+      uint32_t bcount = 0, tcount = 0, nseg = 0;
       const uint32_t a_addr = smem_u32(sA), b_addr = smem_u32(sB);
       bool ok = true;
-      for (int it = it0; it < it1 && ok; ++it) {
-        const Item I = decode_item(P, it);
-        const uint32_t n_local = static_cast<uint32_t>(it - it0);
-        if (!mbar_wait(a_full, n_local & 1u, abort_flag, P.err, ERR_TIMEOUT_MMA, WAIT_LIMIT_NS)) break;
+      for (int it = it0; it < it1 && ok; ++nseg) {
+        const Segment g = next_segment(P, it, it1);
+        it = g.next;
+        if (!mbar_wait(a_full, nseg & 1u, abort_flag, P.err, ERR_TIMEOUT_MMA, WAIT_LIMIT_NS)) break;
         tc_fence_after();
-        for (int ct = I.ct0; ct < I.ct1; ++ct, ++bcount, ++tcount) {
+        for (int ct = g.s.ct0; ct < g.s.ct1; ++ct, ++bcount, ++tcount) {
           const uint32_t st = bcount & 1u, ph = (bcount >> 1) & 1u;
           const uint32_t acc = tcount & 1u, aph = (tcount >> 1) & 1u;
           if (!mbar_wait(&b_full[st], ph, abort_flag, P.err, ERR_TIMEOUT_MMA, WAIT_LIMIT_NS) ||
@@ -233,22 +294,31 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int e = warp - 2;       // 0..7
+    const int e = warp - 2;       // 0..15
     const int q = warp & 3;       // TMEM lane quadrant this warp may read
-    const int h = e >> 2;         // which 128-column half of the tile
+    const int qt = e >> 2;        // which 64-column quarter of the tile
     const uint32_t rl = static_cast<uint32_t>(q * 32 + lane);  // row within the tile
-    const uint32_t rowbits = 127u - rl;
-    const uint32_t hbits = static_cast<uint32_t>(1 - h) << 7;
-    uint32_t* tb = reinterpret_cast<uint32_t*>(smem + OFF_T) + e * T_WARP_WORDS;
-    uint2* sm = reinterpret_cast<uint2*>(smem + OFF_M);
+    const uint32_t col_low = 255u - rl;                         // column keys carry the row
+    const uint32_t r256 = 256u + (blockDim.x >> 16);            // 256, kept in a register
+    const int rd_col = lane & 15, rd_half = lane >> 4;          // transposed read: column, row half
+    // shared-memory addresses (32-bit, shared window) of the transpose block and merge area
+    const uint32_t tb_w = smem_u32(smem + OFF_T) + static_cast<uint32_t>(e * T_WARP_WORDS * 4) + lane * 4;
+    const uint32_t tb_r = smem_u32(smem + OFF_T) + static_cast<uint32_t>(e * T_WARP_WORDS * 4) +
+                          static_cast<uint32_t>((rd_col * T_STRIDE + rd_half * 16) * 4);
+    const uint32_t sm_base = smem_u32(smem + OFF_M);
     uint32_t tcount = 0;
     bool ok = true;
-    for (int it = it0; it < it1 && ok; ++it) {
-      const Item I = decode_item(P, it);
-      const FusedPair& fp = P.pairs[I.p];
-      const int64_t nb_pad = round_up(fp.n_b, PAD_ROWS);
-      uint64_t K1 = 0, K2 = 0;
-      for (int ct = I.ct0; ct < I.ct1; ++ct, ++tcount) {
+    // second-slot update of the previous tile's column, deferred so that the
+    // returning atomic's latency overlaps the next tile
+    unsigned long long* pend_ptr = nullptr;
+    unsigned long long pend_old = 0ull, pend_x1 = 0ull;
+    for (int it = it0; it < it1 && ok;) {
+      const Segment g = next_segment(P, it, it1);
+      it = g.next;
+      const FusedPair& fp = P.pairs[g.s.p];
+      unsigned long long K1 = 0ull, K2 = 0ull;  // the row's top-2 over the segment
+      uint32_t thr = 0;                          // tile keys below this cannot enter
+      for (int ct = g.s.ct0; ct < g.s.ct1; ++ct, ++tcount) {
         const uint32_t acc = tcount & 1u, aph = (tcount >> 1) & 1u;
         if (!warp_wait(&t_full[acc], aph, abort_flag, P.err, ERR_TIMEOUT_EPILOGUE)) {
           ok = false;
@@ -256,74 +326,129 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t par = tcount & 1u;
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + h * 128;
-        uint32_t k1 = 0, k2 = 0;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + qt * 64;
+        float t1 = 0.f, t2 = 0.f;  // the row's top-2 over this tile (8-bit column index)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(taddr + c * 32, v);
           tmem_wait_ld();
-          if (c == 3) {
+          if (c == 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&t_empty[acc]);
           }
           if constexpr (DUMP) {
-            const int row = I.rt * BM + static_cast<int>(rl);
+            const int row = g.s.rt * BM + static_cast<int>(rl);
             if (row < fp.n_a) {
 #pragma unroll
               for (int k = 0; k < 32; ++k) {
-                const int col = ct * BN + h * 128 + c * 32 + k;
-                if (col < fp.n_b) P.dump[static_cast<int64_t>(row) * P.dump_ld + col] = __float2int_rn(__uint_as_float(v[k]));
+                const int col = ct * BN + qt * 64 + c * 32 + k;
+                if (col < fp.n_b)
+                  P.dump[static_cast<int64_t>(row) * P.dump_ld + col] = __float2int_rn(__uint_as_float(v[k]));
               }
             }
           } else {
+            float rk[32];       // row keys, chunk-local index 31 - k
+            uint32_t ckh[16];   // column keys of the second half-block
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
-              const uint32_t u = __float_as_uint(__fadd_rn(__uint_as_float(v[k]), 8388608.0f)) << 8;
-              ins2(k1, k2, u | hbits | static_cast<uint32_t>(127 - c * 32 - k));
-              tb[k * T_STRIDE + lane] = u | rowbits;
+              const uint32_t u = __float_as_uint(__fadd_rn(__uint_as_float(v[k]), 8388608.0f));
+              rk[k] = __uint_as_float(mad_lo(u, r256, 31u - k));
+              const uint32_t ck = mad_lo(u, r256, col_low);
+              if (k < 16) st_shared_u32(tb_w + k * T_STRIDE * 4, ck); else ckh[k - 16] = ck;
             }
-            __syncwarp();
-            uint32_t c1 = 0, c2 = 0;
 #pragma unroll
-            for (int r4 = 0; r4 < 8; ++r4) {
-              const uint4 x = *reinterpret_cast<const uint4*>(tb + lane * T_STRIDE + r4 * 4);
-              ins2(c1, c2, x.x);
-              ins2(c1, c2, x.y);
-              ins2(c1, c2, x.z);
-              ins2(c1, c2, x.w);
+            for (int hb = 0; hb < 2; ++hb) {
+              if (hb == 1) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) st_shared_u32(tb_w + k * T_STRIDE * 4, ckh[k]);
+              }
+              __syncwarp();
+              float xs[16];
+#pragma unroll
+              for (int r4 = 0; r4 < 4; ++r4) {
+                const uint4 x = ld_shared_v4(tb_r + r4 * 16);
+                xs[4 * r4 + 0] = __uint_as_float(x.x);
+                xs[4 * r4 + 1] = __uint_as_float(x.y);
+                xs[4 * r4 + 2] = __uint_as_float(x.z);
+                xs[4 * r4 + 3] = __uint_as_float(x.w);
+              }
+              __syncwarp();
+              float c1, c2;
+              tree_top2(xs, c1, c2);
+              merge2(c1, c2, __shfl_xor_sync(0xffffffffu, c1, 16), __shfl_xor_sync(0xffffffffu, c2, 16));
+              if (lane < 16)
+                st_shared_v2(sm_base + static_cast<uint32_t>(((par * 4 + q) * BN + qt * 64 + c * 32 + hb * 16 + rd_col) * 8),
+                             __float_as_uint(c1), __float_as_uint(c2));
             }
-            __syncwarp();
-            sm[(par * 4 + q) * BN + h * 128 + c * 32 + lane] = make_uint2(c1, c2);
+            float a1, a2;
+            tree_top2(rk, a1, a2);
+            // chunk-local index (31 - k) -> tile-local 255 - (64 qt + 32 c + k)
+            const uint32_t chb = static_cast<uint32_t>(7 - 2 * qt - c) << 5;
+            merge2(t1, t2, __uint_as_float(__float_as_uint(a1) | chb), __uint_as_float(__float_as_uint(a2) | chb));
           }
         }
         if constexpr (!DUMP) {
-          // row: fold this tile's top-2 into the item's running top-2
-          const int col0 = ct * BN;
-          ins2_64(K1, K2, row_key64(k1, col0));
-          ins2_64(K1, K2, row_key64(k2, col0));
+          // row: fold the tile's top-2 into the segment's (rarely taken after a few tiles)
+          const uint32_t k1t = __float_as_uint(t1), k2t = __float_as_uint(t2);
+          if (k1t >= thr) {
+            const uint32_t base = static_cast<uint32_t>(ct * BN);
+            ins2_64(K1, K2, key64(k1t, base));
+            ins2_64(K1, K2, key64(k2t, base));
+            thr = static_cast<uint32_t>(K2 >> 32) << 8;
+          }
           // columns: merge the four row quadrants once all four have written
           __syncwarp();
-          if (lane == 0) mbar_arrive(&merged[par * 2 + h]);
-          if (!warp_wait(&merged[par * 2 + h], (tcount >> 1) & 1u, abort_flag, P.err, ERR_TIMEOUT_EPILOGUE)) {
+          if (lane == 0) mbar_arrive(&merged[par * 4 + qt]);
+          if (!warp_wait(&merged[par * 4 + qt], (tcount >> 1) & 1u, abort_flag, P.err, ERR_TIMEOUT_EPILOGUE)) {
             ok = false;
             break;
           }
-          const int col = h * 128 + q * 32 + lane;
-          uint32_t m1 = 0, m2 = 0;
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            const uint2 x = sm[(par * 4 + qq) * BN + col];
-            ins2(m1, m2, x.x);
-            ins2(m1, m2, x.y);
+          if (pend_ptr) {
+            const unsigned long long lo = pend_old < pend_x1 ? pend_old : pend_x1;
+            if (lo) atomicMax(pend_ptr, lo);
+            pend_ptr = nullptr;
           }
-          P.colpart[fp.colpart_base + static_cast<int64_t>(I.rt) * nb_pad + ct * BN + col] = make_uint2(m1, m2);
+          if (lane < 16) {
+            const int col = qt * 64 + q * 16 + lane;
+            uint2 x = ld_shared_v2(sm_base + static_cast<uint32_t>(((par * 4 + 0) * BN + col) * 8));
+            float m1 = __uint_as_float(x.x), m2 = __uint_as_float(x.y);
+#pragma unroll
+            for (int qq = 1; qq < 4; ++qq) {
+              x = ld_shared_v2(sm_base + static_cast<uint32_t>(((par * 4 + qq) * BN + col) * 8));
+              merge2(m1, m2, __uint_as_float(x.x), __uint_as_float(x.y));
+            }
+            const int j = ct * BN + col;
+            if (j < fp.n_b) {
+              const uint32_t rbase = static_cast<uint32_t>(g.s.rt * BM);
+              const unsigned long long x1 = key64(__float_as_uint(m1), rbase);
+              const unsigned long long x2 = key64(__float_as_uint(m2), rbase);
+              if (x1) {
+                unsigned long long* ck = P.colkeys + 2 * static_cast<int64_t>(fp.col_base + j);
+                pend_old = atomicMax(ck, x1);
+                pend_x1 = x1;
+                pend_ptr = ck + 1;
+                if (x2) atomicMax(ck + 1, x2);
+              }
+            }
+          }
         }
       }
       if constexpr (!DUMP) {
-        if (ok) P.rowpart[(static_cast<int64_t>(it) * 2 + h) * BM + rl] = make_ulonglong2(K1, K2);
+        const int i = g.s.rt * BM + static_cast<int>(rl);
+        if (ok && i < fp.n_a && K1) {
+          unsigned long long* rk = P.rowkeys + 2 * static_cast<int64_t>(fp.row_base + i);
+          const unsigned long long old = atomicMax(rk, K1);
+          const unsigned long long lo = old < K1 ? old : K1;
+          if (lo) atomicMax(rk + 1, lo);
+          if (K2) atomicMax(rk + 1, K2);
+        }
       }
+    }
+    if (pend_ptr) {
+      const unsigned long long lo = pend_old < pend_x1 ? pend_old : pend_x1;
+      if (lo) atomicMax(pend_ptr, lo);
     }
   }
 

@@ -6,10 +6,11 @@
 // one buffer that a single TMA tensor map covers; the zero rows score 0 and the
 // zero floor drops them, so ragged tails need no masking.
 //
-// Work item = (pair, row tile, column split): one A tile resident in shared memory
-// against a contiguous run of B tiles.  Items are cut so that every launch has at
-// least a few items per SM; each CTA of the persistent fused kernel takes a
-// contiguous range of items balanced by tile count.
+// Work item = (pair, row tile, column split).  Items are cut so that every launch
+// has at least a few items per SM; each CTA of the persistent fused kernel takes a
+// contiguous range of items balanced by tile count, and runs of its items on the
+// same row tile form one segment: one A tile resident in shared memory against a
+// contiguous run of B tiles, with one running row top-2.
 #pragma once
 #include <stdint.h>
 
@@ -21,7 +22,7 @@ constexpr int KDIM = 128;        // descriptor length
 constexpr int PAD_ROWS = 256;    // staged images are padded to this many rows
 constexpr int MAX_PAIRS = 128;   // pairs per launch (kernel-parameter tables)
 constexpr int MAX_GRID = 256;    // persistent CTAs per launch
-constexpr int FUSED_THREADS = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int FUSED_THREADS = 576;  // warp 0 TMA, warp 1 MMA, warps 2..17 epilogue
 
 __host__ __device__ inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
@@ -29,6 +30,7 @@ __host__ __device__ inline int64_t round_up(int64_t x, int64_t m) { return (x + 
 constexpr int ERR_TIMEOUT_PRODUCER = 1;
 constexpr int ERR_TIMEOUT_MMA = 2;
 constexpr int ERR_TIMEOUT_EPILOGUE = 4;
+constexpr int ERR_TIMEOUT_LOOKBACK = 8;
 
 struct FusedPair {
   int32_t a_row0;      // first staged row of image A
@@ -36,19 +38,23 @@ struct FusedPair {
   int32_t n_a, n_b;
   int32_t nsplit;      // column splits per row tile (<= column tiles)
   int32_t item_base;   // first work item of this pair
-  int64_t colpart_base;  // first column-partial entry of this pair
+  int32_t row_base;    // first row-key entry of this pair
+  int32_t col_base;    // first column-key entry of this pair
 };
 
+// Final top-2 of a row or column as two 64-bit keys (best, second):
+// key = score << 32 | (0xFFFFFFFF - index), 0 = empty.  A plain unsigned max orders
+// by score, then lower index.  Kernels merge into them with atomicMax.
 struct FusedParams {
   int32_t n_pairs;
   int32_t n_items;
   int32_t grid;
-  int32_t dump_ld;                 // score-dump row stride (dump mode only)
-  uint2* colpart;                  // [pair][row tile][n_b padded] (k1, k2)
-  ulonglong2* rowpart;             // [item][half][128] (K1, K2)
-  int32_t* err;                    // error bits
-  int32_t* dump;                   // score dump (dump mode only)
-  int32_t cta_first[MAX_GRID + 1]; // items [cta_first[c], cta_first[c+1]) go to CTA c
+  int32_t dump_ld;                   // score-dump row stride (dump mode only)
+  unsigned long long* rowkeys;       // [rows of the chunk][2]
+  unsigned long long* colkeys;       // [columns of the chunk][2]
+  int32_t* err;                      // error bits
+  int32_t* dump;                     // score dump (dump mode only)
+  int32_t cta_first[MAX_GRID + 1];   // items [cta_first[c], cta_first[c+1]) go to CTA c
   FusedPair pairs[MAX_PAIRS];
 };
 
@@ -60,17 +66,20 @@ struct StageImage {
 
 struct StageParams {
   int32_t n_images;
-  int32_t max_pad_rows;
-  uint16_t* staged;  // bf16 bits, [rows][128]
+  int32_t zero_blocks;   // blocks of the extra grid row that clears `zero`
+  uint16_t* staged;      // bf16 bits, [rows][128]
+  uint4* zero;           // cleared before the fused kernel (key arrays)
+  int64_t zero_n;        // 16-byte words to clear
+  int32_t* err;          // error word, cleared too
   StageImage images[512];
 };
 
 struct FinishPair {
   int32_t n_a, n_b;
-  int32_t nsplit, item_base;
-  int64_t colpart_base;
-  int32_t row_base;   // first entry of this pair in rowfinal
-  int32_t col_base;   // first entry of this pair in colfinal
+  int32_t row_base;   // first entry of this pair in rowkeys
+  int32_t col_base;   // first entry of this pair in colkeys
+  int32_t blk_base;   // first block (and status word) of this pair in the match launch
+  int32_t nblk;       // blocks of this pair (MATCH_ROWS_PER_BLOCK rows each, at least 1)
   int32_t* matches;
   int32_t* count;
   int32_t* row_top2;
@@ -79,22 +88,27 @@ struct FinishPair {
   int32_t pad_;
 };
 
+constexpr int MATCH_THREADS = 256;
+constexpr int MATCH_ROWS_PER_THREAD = 2;
+constexpr int MATCH_ROWS_PER_BLOCK = MATCH_THREADS * MATCH_ROWS_PER_THREAD;
+
 struct FinishParams {
   int32_t n_pairs;
-  int32_t total_rows, total_cols;
+  int32_t total_blocks;
   int32_t ratio_num_sq, ratio_den_sq, norm_sq, min_score, mutual, col_ratio;
-  const uint2* colpart;
-  const ulonglong2* rowpart;
-  int4* rowfinal;
-  int4* colfinal;
-  const int32_t* err;
+  const unsigned long long* rowkeys;
+  const unsigned long long* colkeys;
+  int32_t* tickets;               // [pair]: next block index of the pair (zeroed)
+  unsigned long long* status;     // [block]: look-back word (zeroed)
+  uint4* zero;                    // the other chunk's key region, cleared here
+  int64_t zero_n;                 // 16-byte words
+  int32_t* err;
   FinishPair pairs[MAX_PAIRS];
 };
 
 // launchers (defined in fused.cu / finish.cu); return a cudaError_t value
 int launch_stage(const StageParams& p, int64_t max_chunks, void* stream);
 int launch_fused(const FusedParams& p, const void* tmap, bool dump, void* stream);
-int launch_reduce(const FinishParams& p, void* stream);
 int launch_match(const FinishParams& p, void* stream);
 int fused_smem_bytes();
 
