@@ -174,7 +174,8 @@ template <bool DUMP>
 __global__ void __launch_bounds__(FUSED_THREADS, 1)
     fused_top2_kernel(const __grid_constant__ FusedParams P, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // align to 1024 B by pointer arithmetic on the shared array (keeps the address space)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem + OFF_A;
   uint8_t* sB = smem + OFF_B;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -184,7 +185,6 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
   uint64_t* b_empty = bars + 4;   // [2]
   uint64_t* t_full = bars + 6;    // [2]
   uint64_t* t_empty = bars + 8;   // [2]
-  uint64_t* merged = bars + 10;   // [parity 2][quarter 4]
   uint64_t* drain = bars + 18;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 20);
@@ -200,7 +200,6 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
       mbar_init(&t_full[i], 1);
       mbar_init(&t_empty[i], NUM_EPI_WARPS);
     }
-    for (int i = 0; i < 8; ++i) mbar_init(&merged[i], 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -299,20 +298,23 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     const int qt = e >> 2;        // which 64-column quarter of the tile
     const uint32_t rl = static_cast<uint32_t>(q * 32 + lane);  // row within the tile
     const uint32_t col_low = 255u - rl;                         // column keys carry the row
-    const uint32_t r256 = 256u + (blockDim.x >> 16);            // 256, kept in a register
+    // 256 in two registers the compiler cannot see through, so each key is one
+    // multiply-add of its own instead of a shared product plus an add
+    const uint32_t r256a = 256u + (blockDim.x >> 16), r256b = 256u + (blockDim.x >> 17);
     const int rd_col = lane & 15, rd_half = lane >> 4;          // transposed read: column, row half
-    // shared-memory addresses (32-bit, shared window) of the transpose block and merge area
-    const uint32_t tb_w = smem_u32(smem + OFF_T) + static_cast<uint32_t>(e * T_WARP_WORDS * 4) + lane * 4;
-    const uint32_t tb_r = smem_u32(smem + OFF_T) + static_cast<uint32_t>(e * T_WARP_WORDS * 4) +
-                          static_cast<uint32_t>((rd_col * T_STRIDE + rd_half * 16) * 4);
-    const uint32_t sm_base = smem_u32(smem + OFF_M);
+    // transpose block: written row-wise (lane = row), read column-wise
+    uint32_t* tb_w = reinterpret_cast<uint32_t*>(smem + OFF_T) + e * T_WARP_WORDS + lane;
+    const uint4* tb_r =
+        reinterpret_cast<const uint4*>(reinterpret_cast<uint32_t*>(smem + OFF_T) + e * T_WARP_WORDS +
+                                       rd_col * T_STRIDE + rd_half * 16);
+    uint2* sm = reinterpret_cast<uint2*>(smem + OFF_M);
     uint32_t tcount = 0;
     bool ok = true;
     // second-slot update of the previous tile's column, deferred so that the
     // returning atomic's latency overlaps the next tile
     unsigned long long* pend_ptr = nullptr;
     unsigned long long pend_old = 0ull, pend_x1 = 0ull;
-    for (int it = it0; it < it1 && ok;) {
+    for (int it = it0; it < it1;) {
       const Segment g = next_segment(P, it, it1);
       it = g.next;
       const FusedPair& fp = P.pairs[g.s.p];
@@ -320,10 +322,9 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
       uint32_t thr = 0;                          // tile keys below this cannot enter
       for (int ct = g.s.ct0; ct < g.s.ct1; ++ct, ++tcount) {
         const uint32_t acc = tcount & 1u, aph = (tcount >> 1) & 1u;
-        if (!warp_wait(&t_full[acc], aph, abort_flag, P.err, ERR_TIMEOUT_EPILOGUE)) {
-          ok = false;
-          break;
-        }
+        // on a timeout keep going (results are flagged invalid): every epilogue warp
+        // must pass the same named-barrier sequence
+        if (!warp_wait(&t_full[acc], aph, abort_flag, P.err, ERR_TIMEOUT_EPILOGUE)) ok = false;
         tc_fence_after();
         const uint32_t par = tcount & 1u;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + qt * 64;
@@ -354,21 +355,21 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
               const uint32_t u = __float_as_uint(__fadd_rn(__uint_as_float(v[k]), 8388608.0f));
-              rk[k] = __uint_as_float(mad_lo(u, r256, 31u - k));
-              const uint32_t ck = mad_lo(u, r256, col_low);
-              if (k < 16) st_shared_u32(tb_w + k * T_STRIDE * 4, ck); else ckh[k - 16] = ck;
+              rk[k] = __uint_as_float(mad_lo(u, r256a, 31u - k));
+              const uint32_t ck = mad_lo(u, r256b, col_low);
+              if (k < 16) tb_w[k * T_STRIDE] = ck; else ckh[k - 16] = ck;
             }
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
               if (hb == 1) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k) st_shared_u32(tb_w + k * T_STRIDE * 4, ckh[k]);
+                for (int k = 0; k < 16; ++k) tb_w[k * T_STRIDE] = ckh[k];
               }
               __syncwarp();
               float xs[16];
 #pragma unroll
               for (int r4 = 0; r4 < 4; ++r4) {
-                const uint4 x = ld_shared_v4(tb_r + r4 * 16);
+                const uint4 x = tb_r[r4];
                 xs[4 * r4 + 0] = __uint_as_float(x.x);
                 xs[4 * r4 + 1] = __uint_as_float(x.y);
                 xs[4 * r4 + 2] = __uint_as_float(x.z);
@@ -379,8 +380,8 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
               tree_top2(xs, c1, c2);
               merge2(c1, c2, __shfl_xor_sync(0xffffffffu, c1, 16), __shfl_xor_sync(0xffffffffu, c2, 16));
               if (lane < 16)
-                st_shared_v2(sm_base + static_cast<uint32_t>(((par * 4 + q) * BN + qt * 64 + c * 32 + hb * 16 + rd_col) * 8),
-                             __float_as_uint(c1), __float_as_uint(c2));
+                sm[(par * 4 + q) * BN + qt * 64 + c * 32 + hb * 16 + rd_col] =
+                    make_uint2(__float_as_uint(c1), __float_as_uint(c2));
             }
             float a1, a2;
             tree_top2(rk, a1, a2);
@@ -399,12 +400,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
             thr = static_cast<uint32_t>(K2 >> 32) << 8;
           }
           // columns: merge the four row quadrants once all four have written
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&merged[par * 4 + qt]);
-          if (!warp_wait(&merged[par * 4 + qt], (tcount >> 1) & 1u, abort_flag, P.err, ERR_TIMEOUT_EPILOGUE)) {
-            ok = false;
-            break;
-          }
+          named_bar_sync(1 + qt, 128);  // the four quadrant warps of this quarter
           if (pend_ptr) {
             const unsigned long long lo = pend_old < pend_x1 ? pend_old : pend_x1;
             if (lo) atomicMax(pend_ptr, lo);
@@ -412,11 +408,11 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
           }
           if (lane < 16) {
             const int col = qt * 64 + q * 16 + lane;
-            uint2 x = ld_shared_v2(sm_base + static_cast<uint32_t>(((par * 4 + 0) * BN + col) * 8));
+            uint2 x = sm[(par * 4 + 0) * BN + col];
             float m1 = __uint_as_float(x.x), m2 = __uint_as_float(x.y);
 #pragma unroll
             for (int qq = 1; qq < 4; ++qq) {
-              x = ld_shared_v2(sm_base + static_cast<uint32_t>(((par * 4 + qq) * BN + col) * 8));
+              x = sm[(par * 4 + qq) * BN + col];
               merge2(m1, m2, __uint_as_float(x.x), __uint_as_float(x.y));
             }
             const int j = ct * BN + col;
