@@ -143,6 +143,10 @@ int serac_device_check(void);
  * (host-side count, for benchmarking). */
 int serac_last_launch_count(void);
 
+/* The cudaError_t value behind the last SERAC_ECUDA this library returned (0 if
+ * none), for diagnostics. */
+int serac_last_cuda_error(void);
+
 /* Size of the library's built-in scratch used by match_pair_noalloc (16 MiB). */
 #define SERAC_NOALLOC_SCRATCH_BYTES (16 << 20)
 

@@ -25,13 +25,17 @@ NOALLOC_SCRATCH_BYTES = 16 << 20  # SERAC_NOALLOC_SCRATCH_BYTES
 EXPORTS = ("serac_default_params", "serac_pair_workspace_size", "match_pair",
            "match_batch_workspace_size", "match_batch", "serac_scores",
            "serac_set_profile_events", "serac_device_check", "serac_last_launch_count",
-           "serac_schedule_describe", "serac_status_str", "match_pair_noalloc")
+           "serac_schedule_describe", "serac_status_str", "match_pair_noalloc",
+           "serac_last_cuda_error")
 
 
 class SeracError(RuntimeError):
     def __init__(self, status: int, what: str = ""):
         self.status = status
-        super().__init__(f"{what}: {status_str(status)} ({status})" if what else status_str(status))
+        msg = f"{what}: {status_str(status)} ({status})" if what else status_str(status)
+        if status == ECUDA:
+            msg += f" [cudaError {int(lib().serac_last_cuda_error())}]"
+        super().__init__(msg)
 
 
 class Params(ctypes.Structure):

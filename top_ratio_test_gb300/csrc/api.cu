@@ -230,6 +230,7 @@ int encode_staged_map(CUtensorMap* map, void* staged, int64_t rows) {
 
 cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
 int g_last_launches = 0;
+int g_last_cuda_error = 0;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -262,7 +263,11 @@ int check_out(const serac_out* o, int32_t n_a, int32_t n_b) {
 
 #define SERAC_TRY_CUDA(x)                              \
   do {                                                 \
-    if ((x) != cudaSuccess) return SERAC_ECUDA;        \
+    const cudaError_t e_ = (x);                        \
+    if (e_ != cudaSuccess) {                           \
+      g_last_cuda_error = static_cast<int>(e_);        \
+      return SERAC_ECUDA;                              \
+    }                                                  \
   } while (0)
 
 // The whole sequence: staging, then per chunk fused -> reduce -> match (or the
@@ -306,7 +311,7 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
       max_chunks = std::max<int64_t>(max_chunks, round_up(pl.images[i].n, PAD_ROWS) * (KDIM / 16));
     }
     if (sp.n_images == 0 && i0 > 0) continue;
-    if (launch_stage(sp, max_chunks, stream) != 0) return SERAC_ECUDA;
+    SERAC_TRY_CUDA(static_cast<cudaError_t>(launch_stage(sp, max_chunks, stream)));
     ++g_last_launches;
   }
 
@@ -328,6 +333,7 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
       fp.err = err;
       fp.dump = dump;
       fp.dump_ld = (dump && n_pairs > 0) ? pairs[0].n_b : 0;
+      fp.key_mult = 256u;
       int np = 0;
       int64_t item_base = 0, rows = 0, cols = 0;
       for (int k = ch.p0; k < ch.p1; ++k) {
@@ -352,7 +358,7 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
       const bool prof = first_fused && g_ev_begin && g_ev_end;
       if (prof)
         SERAC_TRY_CUDA(cudaEventRecordWithFlags(g_ev_begin, static_cast<cudaStream_t>(stream), cudaEventRecordExternal));
-      if (launch_fused(fp, &map, dump != nullptr, stream) != 0) return SERAC_ECUDA;
+      SERAC_TRY_CUDA(static_cast<cudaError_t>(launch_fused(fp, &map, dump != nullptr, stream)));
       ++g_last_launches;
       if (prof)
         SERAC_TRY_CUDA(cudaEventRecordWithFlags(g_ev_end, static_cast<cudaStream_t>(stream), cudaEventRecordExternal));
@@ -399,7 +405,7 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
     fn.n_pairs = np;
     fn.total_blocks = static_cast<int32_t>(blocks);
     if (np > 0) {
-      if (launch_match(fn, stream) != 0) return SERAC_ECUDA;
+      SERAC_TRY_CUDA(static_cast<cudaError_t>(launch_match(fn, stream)));
       ++g_last_launches;
     }
   }
@@ -511,6 +517,8 @@ int serac_device_check(void) {
 }
 
 int serac_last_launch_count(void) { return g_last_launches; }
+
+int serac_last_cuda_error(void) { return g_last_cuda_error; }
 
 int serac_schedule_describe(const serac_pair* pairs, int32_t n_pairs, int32_t grid, int32_t* out_chunks,
                             int32_t* out_items, int32_t* out_nsplit, int32_t* cta_first) {

@@ -14,6 +14,7 @@
 #include <stdint.h>
 
 #include "serac.h"
+#include "ptx.cuh"
 #include "serac_internal.h"
 
 namespace serac {
@@ -83,6 +84,8 @@ __device__ __forceinline__ uint64_t now_ns() {
 }
 
 __global__ void __launch_bounds__(MATCH_THREADS) match_kernel(const __grid_constant__ FinishParams P) {
+  // launched early (programmatic dependent launch): wait for the fused kernel's keys
+  grid_dep_wait();
   // this block's pair
   int lo = 0, hi = P.n_pairs - 1;
   while (lo < hi) {
@@ -214,8 +217,16 @@ int launch_stage(const StageParams& p, int64_t max_chunks, void* stream) {
 
 int launch_match(const FinishParams& p, void* stream) {
   if (p.total_blocks == 0) return 0;
-  match_kernel<<<p.total_blocks, MATCH_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(p);
-  return static_cast<int>(cudaGetLastError());
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.total_blocks);
+  cfg.blockDim = dim3(MATCH_THREADS);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, match_kernel, p));
 }
 
 }  // namespace serac

@@ -17,7 +17,8 @@
 //     integer score ("Exactness": 128 * 255^2 = 8,323,200 cannot overflow);
 //   * sixteen epilogue warps (four per SM sub-partition) read the accumulator
 //     (thread = row, 64 columns each) and
-//       - add 2^23, which turns the f32 score s into the integer bits 0x4B000000 | s,
+//       - read 2^23 + s (the accumulators start at 2^23), whose f32 bits are the
+//         integer 0x4B000000 | s,
 //       - build packed keys s << 8 | index with one integer multiply-add each (the
 //         multiply by 256 shifts the exponent bits out), so a plain max orders by
 //         score then lower index -- the order-independent tie rule of "Real-Time
@@ -213,6 +214,25 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Every accumulator starts at 2^23 and the MMAs accumulate onto it, so the f32
+  // result is 2^23 + s, whose bits are 0x4B000000 | s (s < 2^23; exact: all values stay
+  // integers below 2^24).  The epilogue refills a buffer with 2^23 after reading it.
+  if (warp >= 2) {
+    const int q0 = warp & 3, qt0 = (warp - 2) >> 2;
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        tmem_st_32x32b_x32_fill(tmem_base + (static_cast<uint32_t>(q0 * 32) << 16) + a * BN + qt0 * 64 + c * 32,
+                                0x4B000000u);
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // everything above overlaps the staging kernel (programmatic dependent launch);
+  // the staged operands, the cleared keys and the error word are read after this
+  grid_dep_wait();
 
   const int it0 = P.cta_first[blockIdx.x], it1 = P.cta_first[blockIdx.x + 1];
 
@@ -278,7 +298,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
             const uint32_t koff = static_cast<uint32_t>((kk >> 2) * A_HALF + (kk & 3) * 32);
             const uint32_t kboff = static_cast<uint32_t>((kk >> 2) * B_HALF + (kk & 3) * 32);
             mma_bf16(d, sw128_kmajor_desc(a_addr + koff), sw128_kmajor_desc(b_addr + st * B_BYTES + kboff), IDESC,
-                     kk > 0 ? 1u : 0u);
+                     1u);
           }
           mma_commit(&b_empty[st]);
           mma_commit(&t_full[acc]);
@@ -298,9 +318,10 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     const int qt = e >> 2;        // which 64-column quarter of the tile
     const uint32_t rl = static_cast<uint32_t>(q * 32 + lane);  // row within the tile
     const uint32_t col_low = 255u - rl;                         // column keys carry the row
-    // 256 in two registers the compiler cannot see through, so each key is one
-    // multiply-add of its own instead of a shared product plus an add
-    const uint32_t r256a = 256u + (blockDim.x >> 16), r256b = 256u + (blockDim.x >> 17);
+    // keys are u * 256 + index bits; 256 comes from a kernel parameter so column keys
+    // (register addend) stay one multiply-add on the FMA pipe; row keys (immediate
+    // addend) become one shift-and-add
+    const uint32_t key_mult = P.key_mult;
     const int rd_col = lane & 15, rd_half = lane >> 4;          // transposed read: column, row half
     // transpose block: written row-wise (lane = row), read column-wise
     uint32_t* tb_w = reinterpret_cast<uint32_t*>(smem + OFF_T) + e * T_WARP_WORDS + lane;
@@ -334,11 +355,6 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
           uint32_t v[32];
           tmem_ld_32x32b_x32(taddr + c * 32, v);
           tmem_wait_ld();
-          if (c == 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&t_empty[acc]);
-          }
           if constexpr (DUMP) {
             const int row = g.s.rt * BM + static_cast<int>(rl);
             if (row < fp.n_a) {
@@ -346,25 +362,25 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
               for (int k = 0; k < 32; ++k) {
                 const int col = ct * BN + qt * 64 + c * 32 + k;
                 if (col < fp.n_b)
-                  P.dump[static_cast<int64_t>(row) * P.dump_ld + col] = __float2int_rn(__uint_as_float(v[k]));
+                  P.dump[static_cast<int64_t>(row) * P.dump_ld + col] =
+                      static_cast<int32_t>(v[k] & 0x7FFFFFu);  // bits of 2^23 + s
               }
             }
           } else {
-            float rk[32];       // row keys, chunk-local index 31 - k
-            uint32_t ckh[16];   // column keys of the second half-block
+            // row: keys (chunk-local index 31 - k) reduced first, so they die early
+            float a1, a2;
+            {
+              float rk[32];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const uint32_t u = __float_as_uint(__fadd_rn(__uint_as_float(v[k]), 8388608.0f));
-              rk[k] = __uint_as_float(mad_lo(u, r256a, 31u - k));
-              const uint32_t ck = mad_lo(u, r256b, col_low);
-              if (k < 16) tb_w[k * T_STRIDE] = ck; else ckh[k - 16] = ck;
+              for (int k = 0; k < 32; ++k) rk[k] = __uint_as_float(mad_lo(v[k], key_mult, 31u - k));
+              tree_top2(rk, a1, a2);
             }
+            // columns: keys go straight from the loaded values into the transpose block,
+            // one 16-column half-block at a time
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
-              if (hb == 1) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k) tb_w[k * T_STRIDE] = ckh[k];
-              }
+              for (int k = 0; k < 16; ++k) tb_w[k * T_STRIDE] = mad_lo(v[hb * 16 + k], key_mult, col_low);
               __syncwarp();
               float xs[16];
 #pragma unroll
@@ -383,13 +399,18 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
                 sm[(par * 4 + q) * BN + qt * 64 + c * 32 + hb * 16 + rd_col] =
                     make_uint2(__float_as_uint(c1), __float_as_uint(c2));
             }
-            float a1, a2;
-            tree_top2(rk, a1, a2);
             // chunk-local index (31 - k) -> tile-local 255 - (64 qt + 32 c + k)
             const uint32_t chb = static_cast<uint32_t>(7 - 2 * qt - c) << 5;
             merge2(t1, t2, __uint_as_float(__float_as_uint(a1) | chb), __uint_as_float(__float_as_uint(a2) | chb));
           }
         }
+        // refill this warp's 64 columns with 2^23 and hand the buffer back to the MMA
+        tmem_st_32x32b_x32_fill(taddr, 0x4B000000u);
+        tmem_st_32x32b_x32_fill(taddr + 32, 0x4B000000u);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&t_empty[acc]);
         if constexpr (!DUMP) {
           // row: fold the tile's top-2 into the segment's (rarely taken after a few tiles)
           const uint32_t k1t = __float_as_uint(t1), k2t = __float_as_uint(t2);
@@ -473,12 +494,19 @@ int launch_fused(const FusedParams& p, const void* tmap, bool dump, void* stream
   }
   CUtensorMap map;
   memcpy(&map, tmap, sizeof(map));
-  const dim3 grid(p.grid), block(FUSED_THREADS);
-  if (dump)
-    fused_top2_kernel<true><<<grid, block, SMEM_TOTAL, static_cast<cudaStream_t>(stream)>>>(p, map);
-  else
-    fused_top2_kernel<false><<<grid, block, SMEM_TOTAL, static_cast<cudaStream_t>(stream)>>>(p, map);
-  return static_cast<int>(cudaGetLastError());
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(FUSED_THREADS);
+  cfg.dynamicSmemBytes = SMEM_TOTAL;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = dump ? cudaLaunchKernelEx(&cfg, fused_top2_kernel<true>, p, map)
+           : cudaLaunchKernelEx(&cfg, fused_top2_kernel<false>, p, map);
+  return static_cast<int>(e);
 }
 
 }  // namespace serac

@@ -54,6 +54,7 @@ struct FusedParams {
   unsigned long long* colkeys;       // [columns of the chunk][2]
   int32_t* err;                      // error bits
   int32_t* dump;                     // score dump (dump mode only)
+  uint32_t key_mult;                 // 256, read as a kernel parameter (see the epilogue)
   int32_t cta_first[MAX_GRID + 1];   // items [cta_first[c], cta_first[c+1]) go to CTA c
   FusedPair pairs[MAX_PAIRS];
 };
