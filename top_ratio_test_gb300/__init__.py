@@ -173,16 +173,30 @@ def _make_out(n_a: int, n_b: int, device, capacity: Optional[int], top2: bool):
     return o, c
 
 
+def output_for(o: MatchOutput):
+    """The C-ABI output record of an existing MatchOutput (to reuse its buffers)."""
+    return _Out(o.matches.data_ptr(), o.matches.shape[0], o.count.data_ptr(),
+                o.row_top2.data_ptr() if o.row_top2 is not None else None,
+                o.col_top2.data_ptr() if o.col_top2 is not None else None)
+
+
 def match_pair(a: torch.Tensor, b: torch.Tensor, params: Optional[Params] = None, *,
                capacity: Optional[int] = None, top2: bool = False,
-               workspace_t: Optional[torch.Tensor] = None, stream=None) -> MatchOutput:
-    """Match descriptors a (n_a, 128) against b (n_b, 128), asynchronously."""
+               workspace_t: Optional[torch.Tensor] = None, stream=None,
+               out: Optional[MatchOutput] = None) -> MatchOutput:
+    """Match descriptors a (n_a, 128) against b (n_b, 128), asynchronously.  `out`
+    (from an earlier call with the same sizes) reuses its buffers."""
     a, b = _desc(a, "a"), _desc(b, "b")
     p = params if params is not None else default_params()
     n_a, n_b = a.shape[0], b.shape[0]
-    need = pair_workspace_size(n_a, n_b)
-    ws = workspace_t if workspace_t is not None else workspace(need, a.device)
-    o, c = _make_out(n_a, n_b, a.device, capacity, top2)
+    if workspace_t is not None:
+        ws = workspace_t
+    else:
+        ws = workspace(pair_workspace_size(n_a, n_b), a.device)
+    if out is not None:
+        o, c = out, output_for(out)
+    else:
+        o, c = _make_out(n_a, n_b, a.device, capacity, top2)
     st = lib().match_pair(a.data_ptr(), n_a, b.data_ptr(), n_b, ctypes.byref(p), ctypes.byref(c),
                           ws.data_ptr(), ws.numel(), _stream_ptr(stream))
     _check(st, "match_pair")

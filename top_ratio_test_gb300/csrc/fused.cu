@@ -318,9 +318,10 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     const int qt = e >> 2;        // which 64-column quarter of the tile
     const uint32_t rl = static_cast<uint32_t>(q * 32 + lane);  // row within the tile
     const uint32_t col_low = 255u - rl;                         // column keys carry the row
-    // keys are u * 256 + index bits; 256 comes from a kernel parameter so column keys
-    // (register addend) stay one multiply-add on the FMA pipe; row keys (immediate
-    // addend) become one shift-and-add
+    // keys are u * 256 + index bits (the multiply shifts the exponent bits out).  Row
+    // keys (immediate index) are one shift-and-add on the integer ALU; column keys
+    // (per-thread index) take 256 from a kernel parameter so the compiler keeps them
+    // one multiply-add on the FMA pipe, off the busier ALU
     const uint32_t key_mult = P.key_mult;
     const int rd_col = lane & 15, rd_half = lane >> 4;          // transposed read: column, row half
     // transpose block: written row-wise (lane = row), read column-wise
@@ -372,7 +373,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
             {
               float rk[32];
 #pragma unroll
-              for (int k = 0; k < 32; ++k) rk[k] = __uint_as_float(mad_lo(v[k], key_mult, 31u - k));
+              for (int k = 0; k < 32; ++k) rk[k] = __uint_as_float((v[k] << 8) + (31u - k));
               tree_top2(rk, a1, a2);
             }
             // columns: keys go straight from the loaded values into the transpose block,
