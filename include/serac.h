@@ -27,9 +27,12 @@
  * integer below 2^24.
  *
  * Conventions for every entry point:
- *   - descriptor arrays are DEVICE pointers to n x 128 uint8, row-major, contiguous,
- *     16-byte aligned; they are read only;
- *   - output arrays and the workspace are DEVICE memory owned by the caller;
+ *   - descriptor arrays are n x 128 uint8, row-major, contiguous, 16-byte aligned,
+ *     read only, in memory the GPU can address: device memory, or pinned host memory
+ *     (cudaHostAlloc / cudaHostRegister; the staging kernel then reads it over the
+ *     host link, so no separate host-to-device copy is needed);
+ *   - outputs are caller-owned, in device memory or pinned host memory (the kernels
+ *     then write the results straight to the host); the workspace is device memory;
  *   - calls are asynchronous on `cuda_stream` (a cudaStream_t; NULL = legacy default
  *     stream); results are valid once that stream has synchronised;
  *   - a call returns a status below; a negative status means nothing was enqueued;

@@ -155,6 +155,21 @@ def test_capacity_overflow_and_repeat(serac, oracle_mod):
     assert torch.equal(r1.result(), r2.result())
 
 
+def test_pinned_host_inputs_and_outputs(serac, oracle_mod):
+    """Descriptors in pinned host memory (read by the staging kernel over the host link)
+    and outputs written straight into pinned host memory give the same results."""
+    p = S.make_pair(6, 64, 0, 1500, 1800, 0.3, 0.05)
+    a = torch.from_numpy(p.a).pin_memory()
+    b = torch.from_numpy(p.b).pin_memory()
+    out = serac.match_pair(a, b, host_out=True, top2=True)
+    got = out.result().numpy()
+    ref = oracle_mod.match(p.a, p.b)
+    assert not out.count.is_cuda
+    np.testing.assert_array_equal(got, ref.matches)
+    np.testing.assert_array_equal(out.row_top2.numpy(), ref.row_top2)
+    np.testing.assert_array_equal(out.col_top2.numpy(), ref.col_top2)
+
+
 def test_workspace_too_small(serac):
     a = torch.zeros((10, 128), dtype=torch.uint8, device="cuda")
     ws = torch.empty(1024, dtype=torch.uint8, device="cuda")

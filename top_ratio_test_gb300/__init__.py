@@ -126,8 +126,10 @@ def pair_workspace_size(n_a: int, n_b: int) -> int:
 
 
 def _desc(x: torch.Tensor, name: str) -> torch.Tensor:
-    if x.dtype != torch.uint8 or x.dim() != 2 or x.shape[1] != DIM or not x.is_cuda:
-        raise ValueError(f"{name}: expected a CUDA uint8 tensor of shape (n, {DIM})")
+    """CUDA tensors, or pinned host tensors (the staging kernel reads those directly
+    over the host link)."""
+    if x.dtype != torch.uint8 or x.dim() != 2 or x.shape[1] != DIM or not (x.is_cuda or x.is_pinned()):
+        raise ValueError(f"{name}: expected a CUDA or pinned-host uint8 tensor of shape (n, {DIM})")
     if not x.is_contiguous():
         raise ValueError(f"{name}: must be contiguous")
     return x
@@ -154,6 +156,8 @@ class MatchOutput:
 
     def result(self):
         """Synchronise and return the matches as a (count, 2) int32 CPU tensor."""
+        if not self.count.is_cuda:  # written by the kernels into host memory
+            torch.cuda.synchronize()
         n = int(self.count.item())
         if n < 0:
             raise SeracError(n, "match")
@@ -162,12 +166,17 @@ class MatchOutput:
         return self.matches[:n].cpu()
 
 
-def _make_out(n_a: int, n_b: int, device, capacity: Optional[int], top2: bool):
+def _make_out(n_a: int, n_b: int, device, capacity: Optional[int], top2: bool, host: bool = False):
     cap = n_a if capacity is None else int(capacity)
-    o = MatchOutput(matches=torch.empty((max(cap, 1), 2), dtype=torch.int32, device=device),
-                    count=torch.empty(1, dtype=torch.int32, device=device),
-                    row_top2=torch.empty((max(n_a, 1), 4), dtype=torch.int32, device=device) if top2 else None,
-                    col_top2=torch.empty((max(n_b, 1), 4), dtype=torch.int32, device=device) if top2 else None)
+
+    def buf(shape):
+        if host:  # pinned host memory the kernels write directly
+            return torch.empty(shape, dtype=torch.int32, pin_memory=True)
+        return torch.empty(shape, dtype=torch.int32, device=device)
+
+    o = MatchOutput(matches=buf((max(cap, 1), 2)), count=buf((1,)),
+                    row_top2=buf((max(n_a, 1), 4)) if top2 else None,
+                    col_top2=buf((max(n_b, 1), 4)) if top2 else None)
     c = _Out(o.matches.data_ptr(), cap, o.count.data_ptr(),
              o.row_top2.data_ptr() if top2 else None, o.col_top2.data_ptr() if top2 else None)
     return o, c
@@ -183,20 +192,24 @@ def output_for(o: MatchOutput):
 def match_pair(a: torch.Tensor, b: torch.Tensor, params: Optional[Params] = None, *,
                capacity: Optional[int] = None, top2: bool = False,
                workspace_t: Optional[torch.Tensor] = None, stream=None,
-               out: Optional[MatchOutput] = None) -> MatchOutput:
-    """Match descriptors a (n_a, 128) against b (n_b, 128), asynchronously.  `out`
-    (from an earlier call with the same sizes) reuses its buffers."""
+               out: Optional[MatchOutput] = None, host_out: bool = False) -> MatchOutput:
+    """Match descriptors a (n_a, 128) against b (n_b, 128), asynchronously.
+
+    a and b may be CUDA tensors or pinned host tensors.  `out` (from an earlier call
+    with the same sizes) reuses its buffers; host_out=True puts new outputs in pinned
+    host memory, written by the kernels directly (read them after synchronising)."""
     a, b = _desc(a, "a"), _desc(b, "b")
     p = params if params is not None else default_params()
     n_a, n_b = a.shape[0], b.shape[0]
+    dev = a.device if a.is_cuda else (b.device if b.is_cuda else torch.device("cuda", torch.cuda.current_device()))
     if workspace_t is not None:
         ws = workspace_t
     else:
-        ws = workspace(pair_workspace_size(n_a, n_b), a.device)
+        ws = workspace(pair_workspace_size(n_a, n_b), dev)
     if out is not None:
         o, c = out, output_for(out)
     else:
-        o, c = _make_out(n_a, n_b, a.device, capacity, top2)
+        o, c = _make_out(n_a, n_b, dev, capacity, top2, host=host_out)
     st = lib().match_pair(a.data_ptr(), n_a, b.data_ptr(), n_b, ctypes.byref(p), ctypes.byref(c),
                           ws.data_ptr(), ws.numel(), _stream_ptr(stream))
     _check(st, "match_pair")

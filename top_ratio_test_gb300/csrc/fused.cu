@@ -352,56 +352,51 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + qt * 64;
         float t1 = 0.f, t2 = 0.f;  // the row's top-2 over this tile (8-bit column index)
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(taddr + c * 32, v);
+        for (int c = 0; c < 4; ++c) {  // 16-column sub-chunks of this warp's 64 columns
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(taddr + c * 16, v);
           tmem_wait_ld();
           if constexpr (DUMP) {
             const int row = g.s.rt * BM + static_cast<int>(rl);
             if (row < fp.n_a) {
 #pragma unroll
-              for (int k = 0; k < 32; ++k) {
-                const int col = ct * BN + qt * 64 + c * 32 + k;
+              for (int k = 0; k < 16; ++k) {
+                const int col = ct * BN + qt * 64 + c * 16 + k;
                 if (col < fp.n_b)
                   P.dump[static_cast<int64_t>(row) * P.dump_ld + col] =
                       static_cast<int32_t>(v[k] & 0x7FFFFFu);  // bits of 2^23 + s
               }
             }
           } else {
-            // row: keys (chunk-local index 31 - k) reduced first, so they die early
+            // row: keys (sub-chunk index 15 - k), reduced by a tree
             float a1, a2;
             {
-              float rk[32];
+              float rk[16];
 #pragma unroll
-              for (int k = 0; k < 32; ++k) rk[k] = __uint_as_float((v[k] << 8) + (31u - k));
+              for (int k = 0; k < 16; ++k) rk[k] = __uint_as_float((v[k] << 8) + (15u - k));
               tree_top2(rk, a1, a2);
             }
-            // columns: keys go straight from the loaded values into the transpose block,
-            // one 16-column half-block at a time
+            // columns: the 16 x 32 block goes through shared memory and back transposed
 #pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
+            for (int k = 0; k < 16; ++k) tb_w[k * T_STRIDE] = mad_lo(v[k], key_mult, col_low);
+            __syncwarp();
+            float xs[16];
 #pragma unroll
-              for (int k = 0; k < 16; ++k) tb_w[k * T_STRIDE] = mad_lo(v[hb * 16 + k], key_mult, col_low);
-              __syncwarp();
-              float xs[16];
-#pragma unroll
-              for (int r4 = 0; r4 < 4; ++r4) {
-                const uint4 x = tb_r[r4];
-                xs[4 * r4 + 0] = __uint_as_float(x.x);
-                xs[4 * r4 + 1] = __uint_as_float(x.y);
-                xs[4 * r4 + 2] = __uint_as_float(x.z);
-                xs[4 * r4 + 3] = __uint_as_float(x.w);
-              }
-              __syncwarp();
-              float c1, c2;
-              tree_top2(xs, c1, c2);
-              merge2(c1, c2, __shfl_xor_sync(0xffffffffu, c1, 16), __shfl_xor_sync(0xffffffffu, c2, 16));
-              if (lane < 16)
-                sm[(par * 4 + q) * BN + qt * 64 + c * 32 + hb * 16 + rd_col] =
-                    make_uint2(__float_as_uint(c1), __float_as_uint(c2));
+            for (int r4 = 0; r4 < 4; ++r4) {
+              const uint4 x = tb_r[r4];
+              xs[4 * r4 + 0] = __uint_as_float(x.x);
+              xs[4 * r4 + 1] = __uint_as_float(x.y);
+              xs[4 * r4 + 2] = __uint_as_float(x.z);
+              xs[4 * r4 + 3] = __uint_as_float(x.w);
             }
-            // chunk-local index (31 - k) -> tile-local 255 - (64 qt + 32 c + k)
-            const uint32_t chb = static_cast<uint32_t>(7 - 2 * qt - c) << 5;
+            __syncwarp();
+            float c1, c2;
+            tree_top2(xs, c1, c2);
+            merge2(c1, c2, __shfl_xor_sync(0xffffffffu, c1, 16), __shfl_xor_sync(0xffffffffu, c2, 16));
+            if (lane < 16)
+              sm[(par * 4 + q) * BN + qt * 64 + c * 16 + rd_col] = make_uint2(__float_as_uint(c1), __float_as_uint(c2));
+            // sub-chunk index (15 - k) -> tile-local 255 - (64 qt + 16 c + k)
+            const uint32_t chb = static_cast<uint32_t>(15 - 4 * qt - c) << 4;
             merge2(t1, t2, __uint_as_float(__float_as_uint(a1) | chb), __uint_as_float(__float_as_uint(a2) | chb));
           }
         }
