@@ -44,6 +44,7 @@ UNIT = "pairs/s"
 N_A = N_B = 8192
 OPS_PER_PAIR = 2 * N_A * N_B * 128
 WORKLOAD = "single pair 8192x8192 SIFT-shaped u8 descriptors, 25% planted at sigma 0.08, seed 0"
+WORKLOAD_2000 = "single pair 2000x2000 SIFT-shaped u8 descriptors, 30% planted at sigma 0.05, seed 0"
 
 
 def _peaks():
@@ -136,7 +137,7 @@ def cpu_baseline(a, b, budget_s: float = 12.0):
         n += 1
     dt = time.perf_counter() - t0
     return ref, {"value": n / dt, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
-                 "sample": f"{n} full 8192x8192 pairs (rows and columns, all threads), {dt:.1f} s"}
+                 "sample": f"{n} full {a.shape[0]}x{b.shape[0]} pairs (rows and columns, all threads), {dt:.1f} s"}
 
 
 def run_reference(args):
@@ -200,14 +201,16 @@ def run_ours(args):
     if st != serac.OK:
         raise SystemExit(f"device check failed: {serac.status_str(st)}")
 
-    pair = sift_synth.single_pair_8192(0)
+    pair = sift_synth.single_pair_8192(0) if args.workload == "pair8192" else sift_synth.single_pair_2000(0)
+    n_a, n_b = pair.a.shape[0], pair.b.shape[0]
+    ops_per_pair = 2 * n_a * n_b * 128
     a_host = torch.from_numpy(pair.a).pin_memory()
     b_host = torch.from_numpy(pair.b).pin_memory()
     a = a_host.to(dev)
     b = b_host.to(dev)
     params = serac.default_params()
     stream = torch.cuda.Stream(device=dev)
-    ws = serac.workspace(serac.pair_workspace_size(N_A, N_B), dev)
+    ws = serac.workspace(serac.pair_workspace_size(n_a, n_b), dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     ev_fb = torch.cuda.Event(enable_timing=True)
     ev_fe = torch.cuda.Event(enable_timing=True)
@@ -290,16 +293,17 @@ def run_ours(args):
 
     peak_tflops, _, peak_kind = _peaks()
     fused_ms = statistics.mean(t_fused)
-    achieved = OPS_PER_PAIR / (fused_ms * 1e-3) / 1e12
+    achieved = ops_per_pair / (fused_ms * 1e-3) / 1e12
     value = world * args.steps / (total_ms * 1e-3)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "n_a": N_A, "n_b": N_B, "l2": "flushed before every step (256 MiB write)",
+        "config": {"workload": WORKLOAD if args.workload == "pair8192" else WORKLOAD_2000, "n_a": n_a, "n_b": n_b,
+                   "l2": "flushed before every step (256 MiB write)",
                    "graph": "one CUDA graph per step, replayed; kernels chained by programmatic dependent launch",
                    "parallelism": f"replicas x{world}"},
-        "int8_equiv_tops": value * OPS_PER_PAIR / 1e12,
+        "int8_equiv_tops": value * ops_per_pair / 1e12,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved / peak_tflops, "traffic": None,
                      "kernel": "fused_top2_kernel", "peak_kind": f"bf16 dense burst, {peak_kind}",
@@ -307,7 +311,7 @@ def run_ours(args):
                      "same steps (event nodes in the step graph would serialise its launches)",
                      "ms_per_step_with_events": statistics.mean(t_step_prof)},
         "e2e": {"value": world * e2e_steps / (e2e_ms * 1e-3), "unit": UNIT,
-                "h2d_bytes_per_step": 2 * N_A * 128, "d2h_bytes_per_step": 4 + 8 * int(e2e_out.count.item()),
+                "h2d_bytes_per_step": (n_a + n_b) * 128, "d2h_bytes_per_step": 4 + 8 * int(e2e_out.count.item()),
                 "path": "match_pair on pinned host descriptors, outputs in pinned host memory "
                         "(kernels read and write the host directly)"},
         "gpu_launches": launches * args.steps,
@@ -324,6 +328,106 @@ def run_ours(args):
     return 0
 
 
+def _batch_workload(name):
+    """(description, list of (a, b) numpy pairs sharing image arrays where the workload does)."""
+    import sift_synth
+    if name == "ring12":
+        r = sift_synth.ring_12x8192(0)
+        return ("12 images x 8192 descriptors on a ring (20% shared with 3 neighbours, sigma 0.06), all 66 pairs",
+                r.images, [(int(i), int(j)) for i, j in r.pairs])
+    if name == "survey100":
+        r = sift_synth.survey_100x8192(0)
+        return ("100 images x 8192 descriptors (10% shared with the 6 nearest indices, sigma 0.05), all 4950 pairs",
+                r.images, [(int(i), int(j)) for i, j in r.pairs])
+    sizes = sift_synth.ragged_sizes(0)
+    imgs, pairs = [], []
+    for k in range(sizes.shape[0]):
+        pr = sift_synth.ragged_pair(0, k, sizes)
+        imgs += [pr.a, pr.b]
+        pairs.append((2 * k, 2 * k + 1))
+    return ("256 ragged pairs, 1000..16384 descriptors per image, 15% planted at sigma 0.05", imgs, pairs)
+
+
+def run_batch(args):
+    """One step = match_batch over the whole workload (images staged once per step)."""
+    import numpy as np
+    import torch
+
+    import top_ratio_test_gb300 as serac
+
+    world, rank, local = _dist()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    desc, imgs_np, pairs_idx = _batch_workload(args.workload)
+    imgs = [torch.from_numpy(x).to(dev) for x in imgs_np]
+    pairs = [(imgs[i], imgs[j]) for i, j in pairs_idx]
+    ops = sum(2 * imgs_np[i].shape[0] * imgs_np[j].shape[0] * 128 for i, j in pairs_idx)
+    params = serac.default_params()
+    stream = torch.cuda.Stream(device=dev)
+    ws = serac.workspace(serac.batch_workspace_size(pairs), dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        outs = serac.match_batch(pairs, params, workspace_t=ws, stream=stream)
+        stream.synchronize()
+        launches = serac.last_launch_count()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            outs = serac.match_batch(pairs, params, workspace_t=ws, stream=stream)
+    stream.synchronize()
+    evs = []
+    clocks = ClockSampler("GPU-" + str(torch.cuda.get_device_properties(dev).uuid))
+    clocks.start()
+    for st in range(args.warmup + args.steps):
+        with torch.cuda.stream(stream):
+            flush.fill_(st & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        if st >= args.warmup:
+            evs.append((e0, e1))
+    stream.synchronize()
+    clk = clocks.stop()
+    total_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
+    n_pairs = len(pairs)
+    value = n_pairs * args.steps / (total_ms * 1e-3)
+    tops = ops * args.steps / (total_ms * 1e-3) / 1e12
+    peak_tflops, _, peak_kind = _peaks()
+    line = {"metric": "image pairs/sec (batch), int8-equivalent TOPS", "value": value, "unit": UNIT,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": desc, "pairs": n_pairs,
+                                             "l2": "flushed before every step (256 MiB write)",
+                                             "graph": "one CUDA graph per step (match_batch), replayed"},
+            "int8_equiv_tops": tops,
+            "roofline": {"bound": "tensor", "achieved": tops, "peak": peak_tflops, "unit": "TFLOP/s",
+                         "frac": tops / peak_tflops, "traffic": None,
+                         "kernel": "whole step (all launches of match_batch)",
+                         "peak_kind": f"bf16 dense burst, {peak_kind}"},
+            "e2e": None, "gpu_launches": launches * args.steps, "clocks": clk}
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build_library()
+        rng = np.random.default_rng(0)
+        check = rng.choice(n_pairs, min(6, n_pairs), replace=False)
+        exact = True
+        t0, done_ops, n_done = time.perf_counter(), 0, 0
+        for k in check:
+            i, j = pairs_idx[k]
+            ref = oracle.match(imgs_np[i], imgs_np[j])
+            exact &= bool(np.array_equal(outs[k].result().numpy(), ref.matches))
+            done_ops += 2 * imgs_np[i].shape[0] * imgs_np[j].shape[0] * 128
+            n_done += 1
+        dt = time.perf_counter() - t0
+        line["bit_exact"] = exact
+        line["bit_exact_sample"] = f"{n_done} seeded pairs against the oracle"
+        # pairs/s of the oracle, scaled from the sampled pairs' work to the mean pair
+        line["cpu_baseline"] = {"value": n_done / dt * (done_ops / n_done) / (ops / n_pairs), "unit": UNIT,
+                                "cores": oracle.max_threads(), "kind": "oracle",
+                                "sample": f"{n_done} pairs in {dt:.1f} s, scaled to the workload's mean pair"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -331,12 +435,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["pair8192", "pair2000", "ring12", "ragged256", "survey100"],
+                    default="pair8192", help="pair8192 is the headline; the others are batch lines "
+                    "for the tables (match_batch over the whole workload per step)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
-    return run_ours(args)
+    if args.workload in ("pair8192", "pair2000"):
+        return run_ours(args)
+    return run_batch(args)
 
 
 if __name__ == "__main__":
