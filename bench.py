@@ -2,22 +2,27 @@
 """Benchmark: exhaustive SIFT matching of one 8,192 x 8,192 descriptor pair per step.
 
 One step = one pass of the whole path (staging, fused tensor-core GEMM + row/column
-top-2, partial reduction, ratio / distance / mutual test with compaction) over the
-seeded 8,192 x 8,192 pair (25% planted matches at sigma 0.08).  Inputs are resident
-in HBM when the timed region starts; L2 is flushed (256 MiB write) before every
-timed step, outside the step's events; steps are enqueued back to back (the host
-does not wait for one step before enqueuing the next).  The step is captured once in a CUDA graph
-and replayed; every replay launches the library's own kernels.
+top-2 merged into per-row and per-column keys, ratio / distance / mutual test with
+compaction) over the seeded 8,192 x 8,192 pair (25% planted matches at sigma 0.08).
+Inputs are resident in HBM when the timed region starts; L2 is flushed (256 MiB
+write) before every timed step, outside the step's events; steps are enqueued back
+to back (the host does not wait for one step before enqueuing the next).  The step
+is captured once in a CUDA graph and replayed; every replay launches the library's
+own kernels.
 
 Also reported on the same JSON line:
   roofline      the fused kernel's int8-equivalent TFLOP/s (2 * n_a * n_b * 128 per
                 launch) against the measured bf16 tensor peak, from CUDA events
-                recorded around that launch inside each step;
-  e2e           the same metric through the public API with host buffers: pinned
-                host -> device copy of both images, match_pair, device -> host copy of
-                the count and the match list, all inside the timed region;
+                recorded around that launch in a second pass of the same steps;
+  e2e           the same metric through the public API with host buffers: the
+                descriptors stay in pinned host memory and the staging kernel reads
+                them over the host link, the match kernel writes the count and the
+                match list into pinned host memory, all inside the timed region;
   cpu_baseline  the CPU oracle on this host's cores (full pairs, bounded in time);
   clocks        nvidia-smi samples taken while the timed loop ran.
+
+--workload selects the batch workloads instead (ring, ragged, 100-image survey), one
+match_batch over the whole workload per step, with the same keys.
 
 --impl reference times the CPU oracle itself on the same workload and metric (the
 pages publish no runnable reference for this path; the oracle is the baseline arm).
@@ -57,15 +62,20 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples every 100 ms while running."""
+    """nvidia-smi samples every 100 ms while running.  Samples are time-stamped; those
+    inside the marked timed window are reported as such.  A timed window shorter than
+    the sampling period is followed by an untimed continuation of the same steps (see
+    hold_load) so that the clocks under that load are still seen."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    MIN_WINDOW_S = 0.5
 
     def __init__(self, gpu_id: str):
         self.gpu = gpu_id
         self.proc = None
+        self.window = None
         self.path = os.path.join("/tmp", f"serac_clocks_{os.getpid()}.csv")
 
     def start(self):
@@ -76,6 +86,30 @@ class ClockSampler:
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        # wait for the first sample so that sampling runs before the timed window opens
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and os.path.getsize(self.path) == 0:
+            time.sleep(0.02)
+
+    def mark(self, t0: float, t1: float):
+        self.window = (t0, t1)
+
+    def hold_load(self, fn, t_begin: float):
+        """Run fn (one untimed step, enqueued) until MIN_WINDOW_S has passed since t_begin."""
+        import torch
+        while time.time() - t_begin < self.MIN_WINDOW_S:
+            for _ in range(8):
+                fn()
+            torch.cuda.synchronize()
+
+    @staticmethod
+    def _stamp(x: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(x.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def stop(self):
         if self.proc is None:
@@ -86,25 +120,41 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.close()
-        sm, mx, reasons = [], [], set()
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
+                    rows.append((self._stamp(parts[0]), float(parts[2]), float(parts[3]),
+                                 {n for n, v in zip(names, parts[6:10]) if v.lower() == "active"}))
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        w0, w1 = self.window if self.window else (None, None)
+        inside = [r for r in rows if w0 is not None and r[0] is not None and w0 <= r[0] <= w1]
+        # the timed window and its untimed continuation under the same load
+        loaded = [r for r in rows if w0 is not None and r[0] is not None and r[0] >= w0] or rows
+        use = inside or loaded
+        reasons = set().union(*[r[3] for r in use]) if use else set()
+        out = {"sm_mhz": statistics.median([r[1] for r in use]) if use else None,
+               "sm_max_mhz": max(r[2] for r in use) if use else None,
+               "reasons": sorted(reasons), "samples": len(use), "samples_in_timed_window": len(inside)}
+        if w0 is not None:
+            out["timed_window_ms"] = round((w1 - w0) * 1e3, 1)
+        if not inside:
+            out["note"] = "timed window shorter than the 100 ms sampling period: samples from its untimed continuation"
+        return out
+
+
+def _on_stream(stream, flush, fn):
+    """One untimed step (L2 flush, then fn) on `stream`."""
+    import torch
+    with torch.cuda.stream(stream):
+        flush.fill_(0)
+        fn()
 
 
 def max_over_ranks(x: float, device) -> float:
@@ -268,8 +318,11 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    t_w0 = time.time()
     t_step, _ = timed(g.replay, args.steps, args.warmup)
     torch.cuda.synchronize()
+    clocks.mark(t_w0, time.time())
+    clocks.hold_load(lambda: _on_stream(stream, flush, g.replay), t_w0)
     clk = clocks.stop()
     t_step_prof, t_fused = timed(g_prof.replay, args.steps, args.warmup, fused_events=True)
 
@@ -376,6 +429,7 @@ def run_batch(args):
     evs = []
     clocks = ClockSampler("GPU-" + str(torch.cuda.get_device_properties(dev).uuid))
     clocks.start()
+    t_w0 = time.time()
     for st in range(args.warmup + args.steps):
         with torch.cuda.stream(stream):
             flush.fill_(st & 0xFF)
@@ -386,6 +440,8 @@ def run_batch(args):
         if st >= args.warmup:
             evs.append((e0, e1))
     stream.synchronize()
+    clocks.mark(t_w0, time.time())
+    clocks.hold_load(lambda: _on_stream(stream, flush, g.replay), t_w0)
     clk = clocks.stop()
     total_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
     n_pairs = len(pairs)
@@ -404,6 +460,35 @@ def run_batch(args):
                          "kernel": "whole step (all launches of match_batch)",
                          "peak_kind": f"bf16 dense burst, {peak_kind}"},
             "e2e": None, "gpu_launches": launches * args.steps, "clocks": clk}
+    # e2e through the public API from host buffers: the images stay in pinned host
+    # memory (the staging kernel reads each image once per step over the host link)
+    # and the kernels write counts and match lists straight into pinned host memory
+    imgs_host = [torch.from_numpy(x).pin_memory() for x in imgs_np]
+    pairs_host = [(imgs_host[i], imgs_host[j]) for i, j in pairs_idx]
+    ws_h = serac.workspace(serac.batch_workspace_size(pairs_host), dev)
+    with torch.cuda.stream(stream):
+        e2e_outs = serac.match_batch(pairs_host, params, workspace_t=ws_h, stream=stream, host_out=True)
+    stream.synchronize()
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_evs = []
+    for st in range(3 + e2e_steps):
+        with torch.cuda.stream(stream):
+            flush.fill_(st & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            serac.match_batch(pairs_host, params, workspace_t=ws_h, stream=stream, outs=e2e_outs)
+            e1.record(stream)
+        if st >= 3:
+            e2e_evs.append((e0, e1))
+    stream.synchronize()
+    e2e_ms = sum(e0.elapsed_time(e1) for e0, e1 in e2e_evs)
+    same = all(torch.equal(o.result(), h.result()) for o, h in zip(outs, e2e_outs))
+    line["e2e"] = {"value": n_pairs * e2e_steps / (e2e_ms * 1e-3), "unit": UNIT,
+                   "h2d_bytes_per_step": sum(x.shape[0] * 128 for x in imgs_np),
+                   "d2h_bytes_per_step": sum(4 + 8 * int(h.count.item()) for h in e2e_outs),
+                   "steps": e2e_steps, "equals_device_resident_result": bool(same),
+                   "path": "match_batch on pinned host images, outputs in pinned host memory "
+                           "(kernels read and write the host directly)"}
     if not args.no_cpu_baseline:
         import oracle
         oracle.build_library()

@@ -150,6 +150,16 @@ int serac_last_launch_count(void);
  * none), for diagnostics. */
 int serac_last_cuda_error(void);
 
+/* Failure-detection test hook.  With enable != 0, the next match_pair / match_batch
+ * call (its first fused launch only) runs with a TMA producer that issues no copies:
+ * the MMA thread's bounded wait on the operands runs out after its limit (2 s of GPU
+ * time), the kernel records the timeout in the error word and winds down, and the
+ * call reports SERAC_ETIMEOUT through *count; its other outputs are not valid.  No
+ * fault, trap or unbounded wait is involved and the context stays usable: the next
+ * call runs normally.  The flag is consumed by that one call; enable = 0 clears it.
+ * Process-wide, not thread-safe.  Host only; always returns SERAC_OK. */
+int serac_test_inject_timeout(int enable);
+
 /* Size of the library's built-in scratch used by match_pair_noalloc (16 MiB). */
 #define SERAC_NOALLOC_SCRATCH_BYTES (16 << 20)
 

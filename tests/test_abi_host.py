@@ -122,3 +122,11 @@ def test_schedule_large_batch_chunks(serac):
     # at most 128 pairs per launch chunk (their tables travel as kernel parameters)
     assert chunks == 3
     assert nsplit[0] == 1 and items == 128 * 64
+
+
+def test_timeout_hook_is_host_only(serac):
+    """The failure-detection hook only sets a host flag (the GPU test consumes it);
+    clearing it leaves the next call untouched."""
+    L = serac.lib()
+    assert L.serac_test_inject_timeout(1) == 0
+    assert L.serac_test_inject_timeout(0) == 0

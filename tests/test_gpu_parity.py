@@ -203,6 +203,31 @@ def test_batch_ring_12(serac, oracle_mod):
         np.testing.assert_array_equal(outs[k].result().numpy(), ref.matches)
 
 
+def test_batch_host_buffers_and_reuse(serac, oracle_mod):
+    """match_batch on pinned host images (shared between pairs), outputs in pinned
+    host memory, then a second call into the same outputs: both equal the oracle."""
+    imgs_np = [S.make_pair(7, 70, k, 900 + 300 * k, 10, 0.0, 0.05).a for k in range(4)]
+    for k in range(3):  # plant rows of image k into image k + 1
+        imgs_np[k + 1][: 200] = imgs_np[k][100:300]
+    imgs = [torch.from_numpy(x).pin_memory() for x in imgs_np]
+    idx = [(0, 1), (1, 2), (2, 3), (0, 3), (3, 0)]
+    pairs = [(imgs[i], imgs[j]) for i, j in idx]
+    outs = serac.match_batch(pairs, host_out=True, top2=True)
+    torch.cuda.synchronize()
+    for rep in range(2):
+        for k, (i, j) in enumerate(idx):
+            ref = oracle_mod.match(imgs_np[i], imgs_np[j])
+            assert not outs[k].count.is_cuda
+            np.testing.assert_array_equal(outs[k].row_top2.numpy(), ref.row_top2)
+            np.testing.assert_array_equal(outs[k].col_top2.numpy(), ref.col_top2)
+            np.testing.assert_array_equal(outs[k].result().numpy(), ref.matches)
+        for o in outs:
+            o.count.fill_(-99)
+            o.row_top2.fill_(-7)
+        outs = serac.match_batch(pairs, outs=outs)
+        torch.cuda.synchronize()
+
+
 def test_batch_ragged_256(serac, oracle_mod):
     """256 ragged pairs (1,000..16,384 features): 12 pairs checked in full, every
     pair checked on 48 sampled rows (top-2 and decision) and 48 sampled columns."""

@@ -26,7 +26,7 @@ EXPORTS = ("serac_default_params", "serac_pair_workspace_size", "match_pair",
            "match_batch_workspace_size", "match_batch", "serac_scores",
            "serac_set_profile_events", "serac_device_check", "serac_last_launch_count",
            "serac_schedule_describe", "serac_status_str", "match_pair_noalloc",
-           "serac_last_cuda_error")
+           "serac_last_cuda_error", "serac_test_inject_timeout")
 
 
 class SeracError(RuntimeError):
@@ -83,6 +83,7 @@ def lib() -> ctypes.CDLL:
         L.serac_schedule_describe.argtypes = [ctypes.POINTER(_Pair), i32, i32, P, P, P, P]
         L.serac_status_str.restype = ctypes.c_char_p
         L.match_pair_noalloc.argtypes = [P, i32, P, i32, ctypes.POINTER(Params), ctypes.POINTER(_Out), P]
+        L.serac_test_inject_timeout.argtypes = [ctypes.c_int]
         _lib_handle = L
     return _lib_handle
 
@@ -110,6 +111,12 @@ def device_check() -> int:
 
 def last_launch_count() -> int:
     return int(lib().serac_last_launch_count())
+
+
+def inject_timeout(enable: bool = True) -> None:
+    """Failure-detection test hook: the next call's TMA producer issues no copies, so
+    its bounded waits run out (2 s) and the call reports ETIMEOUT through `count`."""
+    lib().serac_test_inject_timeout(1 if enable else 0)
 
 
 def set_profile_events(begin: Optional[torch.cuda.Event], end: Optional[torch.cuda.Event]) -> None:
@@ -246,23 +253,37 @@ def batch_workspace_size(pairs: Sequence) -> int:
 
 def match_batch(pairs: Sequence, params: Optional[Params] = None, *, capacities=None,
                 top2: bool = False, workspace_t: Optional[torch.Tensor] = None,
-                stream=None) -> list:
-    """Match every (a, b) of `pairs`; images shared between pairs are staged once."""
+                stream=None, outs: Optional[list] = None, host_out: bool = False) -> list:
+    """Match every (a, b) of `pairs`; images shared between pairs are staged once.
+
+    Images may be CUDA tensors or pinned host tensors.  `outs` (from an earlier call
+    with the same pairs) reuses those buffers; host_out=True puts new outputs in
+    pinned host memory, written by the kernels directly (read them after
+    synchronising)."""
     arr = _pairs_struct(pairs)
     p = params if params is not None else default_params()
     n = len(pairs)
+    if outs is not None and len(outs) != n:
+        raise ValueError("outs: one MatchOutput per pair expected")
     need = int(lib().match_batch_workspace_size(arr, n))
-    dev = pairs[0][0].device if n else torch.device("cuda")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    for a, b in pairs:
+        if a.is_cuda:
+            dev = a.device
+            break
     ws = workspace_t if workspace_t is not None else workspace(need, dev)
-    outs, couts = [], (_Out * max(n, 1))()
+    res, couts = [], (_Out * max(n, 1))()
     for k, (a, b) in enumerate(pairs):
-        cap = None if capacities is None else capacities[k]
-        o, c = _make_out(a.shape[0], b.shape[0], a.device, cap, top2)
-        outs.append(o)
+        if outs is not None:
+            o, c = outs[k], output_for(outs[k])
+        else:
+            cap = None if capacities is None else capacities[k]
+            o, c = _make_out(a.shape[0], b.shape[0], dev, cap, top2, host=host_out)
+        res.append(o)
         couts[k] = c
     st = lib().match_batch(arr, n, ctypes.byref(p), couts, ws.data_ptr(), ws.numel(), _stream_ptr(stream))
     _check(st, "match_batch")
-    return outs
+    return res
 
 
 def scores(a: torch.Tensor, b: torch.Tensor, *, workspace_t: Optional[torch.Tensor] = None,

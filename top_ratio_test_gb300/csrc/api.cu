@@ -229,6 +229,7 @@ int encode_staged_map(CUtensorMap* map, void* staged, int64_t rows) {
 }
 
 cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
+bool g_inject_no_copies = false;  // consumed by the next call's first fused launch
 int g_last_launches = 0;
 int g_last_cuda_error = 0;
 
@@ -270,8 +271,8 @@ int check_out(const serac_out* o, int32_t n_a, int32_t n_b) {
     }                                                  \
   } while (0)
 
-// The whole sequence: staging, then per chunk fused -> reduce -> match (or the
-// score dump when `dump` is set).
+// The whole sequence: staging, then per chunk fused -> match (or the score dump
+// when `dump` is set).
 int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, const serac_out* outs,
         int32_t* dump, void* workspace, size_t ws_bytes, void* stream) {
   g_last_launches = 0;
@@ -334,6 +335,8 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
       fp.dump = dump;
       fp.dump_ld = (dump && n_pairs > 0) ? pairs[0].n_b : 0;
       fp.key_mult = 256u;
+      fp.no_copies = (first_fused && g_inject_no_copies) ? 1 : 0;
+      if (first_fused) g_inject_no_copies = false;
       int np = 0;
       int64_t item_base = 0, rows = 0, cols = 0;
       for (int k = ch.p0; k < ch.p1; ++k) {
@@ -508,6 +511,11 @@ int serac_scores(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b, int3
 int serac_set_profile_events(void* ev_begin, void* ev_end) {
   g_ev_begin = static_cast<cudaEvent_t>(ev_begin);
   g_ev_end = static_cast<cudaEvent_t>(ev_end);
+  return SERAC_OK;
+}
+
+int serac_test_inject_timeout(int enable) {
+  g_inject_no_copies = enable != 0;
   return SERAC_OK;
 }
 

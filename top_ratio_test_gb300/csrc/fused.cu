@@ -238,7 +238,9 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // (no_copies: the failure-detection test hook -- nothing is loaded, so the MMA's
+    // bounded wait runs out and the call reports a timeout)
+    if (lane == 0 && !P.no_copies) {
       uint32_t bcount = 0, nseg = 0;
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++nseg) {

@@ -55,6 +55,7 @@ struct FusedParams {
   int32_t* err;                      // error bits
   int32_t* dump;                     // score dump (dump mode only)
   uint32_t key_mult;                 // 256, read as a kernel parameter (see the epilogue)
+  int32_t no_copies;                 // test hook: the producer issues no copies (bounded waits run out)
   int32_t cta_first[MAX_GRID + 1];   // items [cta_first[c], cta_first[c+1]) go to CTA c
   FusedPair pairs[MAX_PAIRS];
 };
