@@ -17,16 +17,16 @@
 //     integer score ("Exactness": 128 * 255^2 = 8,323,200 cannot overflow);
 //   * sixteen epilogue warps (four per SM sub-partition) read the accumulator
 //     (thread = row, 64 columns each) and
-//       - read 2^23 + s (the accumulators start at 2^23), whose f32 bits are the
-//         integer 0x4B000000 | s,
-//       - build packed keys s << 8 | index with one integer multiply-add each (the
-//         multiply by 256 shifts the exponent bits out), so a plain max orders by
+//       - read 2^23 + s (each tile's first MMA writes 2^23 from two small bias
+//         operands), whose f32 bits are the integer 0x4B000000 | s,
+//       - build packed keys s << 8 | index with one integer operation each (the
+//         shift by 8 drops the exponent bits), so a plain max orders by
 //         score then lower index -- the order-independent tie rule of "Real-Time
 //         Dense Stereo at 34 Hz on a Jetson TX2 (MASDA, Part 3)", section 6, which
 //         packs (value, k) into one integer for its fused warp top-2.  Every key is
 //         below 0x7F800000, so keys also compare correctly as finite floats and the
 //         3-input float max can merge them;
-//       - reduce each 32-key chunk with a tree (for instruction-level parallelism)
+//       - reduce each 16-key sub-chunk with a tree (for instruction-level parallelism)
 //         and keep the row top-2 in registers across the segment,
 //       - transpose column keys through shared memory in 16-column half-blocks,
 //         take the top-2 of every column over the warp's 32 rows (two lanes per
@@ -69,7 +69,12 @@ constexpr int OFF_M = OFF_T + NUM_EPI_WARPS * T_WARP_WORDS * 4;
 constexpr int M_BYTES = 2 * 4 * BN * 8;  // [parity][quadrant][column] (k1, k2)
 constexpr int OFF_BAR = OFF_M + M_BYTES;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_TOTAL = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
+// bias operands of the first MMA of every tile (no swizzle, one 8-row group read by
+// every group): A_bias rows [1, 0, ..., 0], B_bias rows [2^23, 0, ..., 0], each two K
+// core matrices of 128 bytes
+constexpr int OFF_BIAS = OFF_BAR + BAR_BYTES;
+constexpr int BIAS_BYTES = 512;
+constexpr int SMEM_TOTAL = OFF_BIAS + BIAS_BYTES + 1024;  // + alignment slack
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 
 constexpr uint32_t TMEM_COLS = 512;
@@ -214,22 +219,21 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // Every accumulator starts at 2^23 and the MMAs accumulate onto it, so the f32
-  // result is 2^23 + s, whose bits are 0x4B000000 | s (s < 2^23; exact: all values stay
-  // integers below 2^24).  The epilogue refills a buffer with 2^23 after reading it.
-  if (warp >= 2) {
-    const int q0 = warp & 3, qt0 = (warp - 2) >> 2;
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-        tmem_st_32x32b_x32_fill(tmem_base + (static_cast<uint32_t>(q0 * 32) << 16) + a * BN + qt0 * 64 + c * 32,
-                                0x4B000000u);
-    tmem_wait_st();
+  // Every tile starts with one MMA of the bias operands that overwrites the
+  // accumulator with 1 * 2^23 in every element; the eight real K steps accumulate onto
+  // it, so the f32 result is 2^23 + s, whose bits are the integer 0x4B000000 | s
+  // (s < 2^23; exact: all values stay integers below 2^24).  No per-score add and no
+  // refill of TMEM by the epilogue.  Bias core matrices: eight 16-byte rows each,
+  // element 0 of every row set in the K 0..7 matrix (words 0..31), the K 8..15 matrix
+  // (words 32..63) all zero.
+  if (threadIdx.x < 64) {
+    uint32_t* bias = reinterpret_cast<uint32_t*>(smem + OFF_BIAS);
+    const int w = threadIdx.x;
+    bias[w] = (w < 32 && (w & 3) == 0) ? 0x00003F80u : 0u;        // bf16 1.0
+    bias[64 + w] = (w < 32 && (w & 3) == 0) ? 0x00004B00u : 0u;   // bf16 2^23
+    fence_proxy_async_smem();
   }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
   // everything above overlaps the staging kernel (programmatic dependent launch);
   // the staged operands, the cleared keys and the error word are read after this
   grid_dep_wait();
@@ -279,6 +283,9 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     if (lane == 0) {
       uint32_t bcount = 0, tcount = 0, nseg = 0;
       const uint32_t a_addr = smem_u32(sA), b_addr = smem_u32(sB);
+      const uint32_t bias_addr = smem_u32(smem + OFF_BIAS);
+      const uint64_t a_bias = plain_kmajor_desc(bias_addr, 128, 0);
+      const uint64_t b_bias = plain_kmajor_desc(bias_addr + 256, 128, 0);
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++nseg) {
         const Segment g = next_segment(P, it, it1);
@@ -295,6 +302,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t d = tmem_base + acc * BN;
+          mma_bf16(d, a_bias, b_bias, IDESC, 0u);  // every element = 2^23
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t koff = static_cast<uint32_t>((kk >> 2) * A_HALF + (kk & 3) * 32);
@@ -402,10 +410,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
             merge2(t1, t2, __uint_as_float(__float_as_uint(a1) | chb), __uint_as_float(__float_as_uint(a2) | chb));
           }
         }
-        // refill this warp's 64 columns with 2^23 and hand the buffer back to the MMA
-        tmem_st_32x32b_x32_fill(taddr, 0x4B000000u);
-        tmem_st_32x32b_x32_fill(taddr + 32, 0x4B000000u);
-        tmem_wait_st();
+        // hand the buffer back to the MMA
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&t_empty[acc]);
