@@ -22,6 +22,7 @@ namespace serac {
 namespace {
 
 __global__ void __launch_bounds__(256) stage_kernel(const __grid_constant__ StageParams P) {
+  grid_dep_launch();  // the fused kernel may start its prologue alongside the last blocks
   if (blockIdx.y == static_cast<unsigned>(P.n_images)) {
     // clear the key arrays and the error word
     if (blockIdx.x >= static_cast<unsigned>(P.zero_blocks)) return;
@@ -146,31 +147,44 @@ __global__ void __launch_bounds__(MATCH_THREADS) match_kernel(const __grid_const
       if (lane >= d) s += y;
     }
     if (lane < NW) warp_off[lane] = s - v;
-    if (lane == 31) {
-      // decoupled look-back over the pair's earlier blocks
-      const int total = s;
-      unsigned long long* st = P.status + fp.blk_base;
-      int prefix = 0;
-      if (b == 0) {
-        atomicExch(&st[0], LB_INCL | static_cast<uint32_t>(total));
-      } else {
-        atomicExch(&st[b], LB_AGG | static_cast<uint32_t>(total));
-        const uint64_t t0 = now_ns();
-        for (int k = b - 1; k >= 0;) {
-          const unsigned long long wv = *reinterpret_cast<volatile unsigned long long*>(&st[k]);
-          if (wv == 0ull) {
+    // decoupled look-back over the pair's earlier blocks, 32 at a time: lane i reads
+    // the status word of block k0 - i; the nearest block with an inclusive prefix
+    // ends the walk, the aggregates of the blocks after it are added to that prefix
+    const int total = __shfl_sync(0xffffffffu, s, 31);
+    unsigned long long* st = P.status + fp.blk_base;
+    int prefix = 0;
+    if (b == 0) {
+      if (lane == 0) atomicExch(&st[0], LB_INCL | static_cast<uint32_t>(total));
+    } else {
+      if (lane == 0) atomicExch(&st[b], LB_AGG | static_cast<uint32_t>(total));
+      const uint64_t t0 = now_ns();
+      for (int k0 = b - 1; k0 >= 0; k0 -= 32) {
+        const int k = k0 - lane;
+        unsigned long long wv = LB_INCL;  // before block 0: an inclusive prefix of 0
+        bool late = false;
+        if (k >= 0) {
+          wv = *reinterpret_cast<volatile unsigned long long*>(&st[k]);
+          while (wv == 0ull) {  // every block before this one holds a ticket and publishes
             if (now_ns() - t0 > LB_LIMIT_NS) {
-              atomicOr(P.err, ERR_TIMEOUT_LOOKBACK);
+              late = true;
               break;
             }
-            continue;
+            wv = *reinterpret_cast<volatile unsigned long long*>(&st[k]);
           }
-          prefix += static_cast<int>(static_cast<uint32_t>(wv));
-          if ((wv & ~0xFFFFFFFFull) == LB_INCL) break;
-          --k;
         }
-        atomicExch(&st[b], LB_INCL | static_cast<uint32_t>(prefix + total));
+        if (__any_sync(0xffffffffu, late)) {
+          if (lane == 0) atomicOr(P.err, ERR_TIMEOUT_LOOKBACK);
+          break;
+        }
+        const unsigned incl = __ballot_sync(0xffffffffu, (wv & ~0xFFFFFFFFull) == LB_INCL);
+        const int stop = incl ? __ffs(incl) - 1 : 31;
+        const int val = (lane <= stop) ? static_cast<int>(static_cast<uint32_t>(wv)) : 0;
+        prefix += __reduce_add_sync(0xffffffffu, val);
+        if (incl) break;
       }
+      if (lane == 0) atomicExch(&st[b], LB_INCL | static_cast<uint32_t>(prefix + total));
+    }
+    if (lane == 0) {
       s_prefix = prefix;
       if (b == fp.nblk - 1) *fp.count = (*reinterpret_cast<volatile int32_t*>(P.err) != 0) ? SERAC_ETIMEOUT : prefix + total;
     }

@@ -19,6 +19,10 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Programmatic dependent launch: block until the preceding grid in the stream has
 // completed and its memory operations are visible.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel in the stream (launched with programmatic stream serialisation)
+// be scheduled now; it still waits in grid_dep_wait for this grid's completion and
+// memory before reading anything this grid writes.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
