@@ -50,6 +50,10 @@ N_A = N_B = 8192
 OPS_PER_PAIR = 2 * N_A * N_B * 128
 WORKLOAD = "single pair 8192x8192 SIFT-shaped u8 descriptors, 25% planted at sigma 0.08, seed 0"
 WORKLOAD_2000 = "single pair 2000x2000 SIFT-shaped u8 descriptors, 30% planted at sigma 0.05, seed 0"
+# DRAM bytes (read + write) of one fused_top2_kernel launch on the 8192 x 8192 pair, from
+# the ncu capture summarised in profiles/fused_top2_pair_8192x8192_full.md; None whenever
+# the kernel has changed since that capture
+FUSED_TRAFFIC_8192 = 4498944
 
 
 def _peaks():
@@ -176,13 +180,13 @@ def _dist():
 
 
 def cpu_baseline(a, b, budget_s: float = 12.0):
-    """The oracle as it stands on this host: full pairs, repeated within a time budget."""
+    """The oracle as it stands on this host: full pairs, repeated for about budget_s."""
     import oracle
     oracle.build_library()
     t0 = time.perf_counter()
     ref = oracle.match(a, b)
     n = 1
-    while time.perf_counter() - t0 < budget_s * 0.5:
+    while time.perf_counter() - t0 < budget_s:
         oracle.match(a, b)
         n += 1
     dt = time.perf_counter() - t0
@@ -358,7 +362,8 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}"},
         "int8_equiv_tops": value * ops_per_pair / 1e12,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tflops, "traffic": None,
+                     "frac": achieved / peak_tflops,
+                     "traffic": FUSED_TRAFFIC_8192 if args.workload == "pair8192" else None,
                      "kernel": "fused_top2_kernel", "peak_kind": f"bf16 dense burst, {peak_kind}",
                      "fused_ms": fused_ms, "timing": "fused-kernel events in a second timed pass of the "
                      "same steps (event nodes in the step graph would serialise its launches)",
