@@ -116,6 +116,41 @@ def test_largest_size(serac, oracle_mod):
     _assert_pair(serac, oracle_mod, p.a, p.b)
 
 
+@pytest.mark.parametrize("na,nb", [(128, 65536), (100, 40000), (65536, 200), (40000, 130)])
+def test_extreme_aspect(serac, oracle_mod, na, nb):
+    """One row tile against hundreds of column tiles (every tile its own work item, rows
+    merged across many CTAs), and the transpose (hundreds of row tiles, one column tile)."""
+    p = S.make_pair(4, 63, na + nb, na, nb, 0.3, 0.05)
+    _assert_pair(serac, oracle_mod, p.a, p.b)
+
+
+def test_zero_and_identical_images(serac, oracle_mod):
+    """All-zero descriptors score 0 everywhere (no candidate, no match); an image
+    matched against itself has exact ties wherever rows repeat."""
+    z = np.zeros((300, 128), np.uint8)
+    p = S.make_pair(5, 64, 0, 700, 10, 0.0, 0.05)
+    a = p.a.copy()
+    a[100:140] = a[5]                     # 41 identical rows
+    out, ref = _assert_pair(serac, oracle_mod, z, a)
+    assert len(ref.matches) == 0 and (out.row_top2.cpu().numpy() == [0, -1, 0, -1]).all()
+    _assert_pair(serac, oracle_mod, a, z)
+    _assert_pair(serac, oracle_mod, a, a)
+
+
+def test_batch_many_images_and_chunks(serac, oracle_mod):
+    """300 pairs of 600 distinct small images: two staging launches (512 images each at
+    most) and three launch chunks alternating between the two key regions."""
+    pairs_np = [S.make_pair(6, 65, k, 40 + (k * 37) % 300, 30 + (k * 53) % 290, 0.3, 0.05) for k in range(300)]
+    dev = [(_dev(p.a), _dev(p.b)) for p in pairs_np]
+    outs = serac.match_batch(dev, top2=True)
+    torch.cuda.synchronize()
+    for k, p in enumerate(pairs_np):
+        ref = oracle_mod.match(p.a, p.b)
+        np.testing.assert_array_equal(outs[k].row_top2.cpu().numpy()[:p.a.shape[0]], ref.row_top2)
+        np.testing.assert_array_equal(outs[k].col_top2.cpu().numpy()[:p.b.shape[0]], ref.col_top2)
+        np.testing.assert_array_equal(outs[k].result().numpy(), ref.matches)
+
+
 @pytest.mark.parametrize("variant", ["default", "no_col_ratio", "no_mutual", "loose"])
 def test_ties_and_params(serac, oracle_mod, variant):
     rng = np.random.default_rng(11)
