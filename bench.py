@@ -414,6 +414,10 @@ def run_batch(args):
     import top_ratio_test_gb300 as serac
 
     world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
     desc, imgs_np, pairs_idx = _batch_workload(args.workload)
     imgs = [torch.from_numpy(x).to(dev) for x in imgs_np]
@@ -434,6 +438,9 @@ def run_batch(args):
     evs = []
     clocks = ClockSampler("GPU-" + str(torch.cuda.get_device_properties(dev).uuid))
     clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
     t_w0 = time.time()
     for st in range(args.warmup + args.steps):
         with torch.cuda.stream(stream):
@@ -448,20 +455,21 @@ def run_batch(args):
     clocks.mark(t_w0, time.time())
     clocks.hold_load(lambda: _on_stream(stream, flush, g.replay), t_w0)
     clk = clocks.stop()
-    total_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
+    total_ms = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in evs), dev)
     n_pairs = len(pairs)
-    value = n_pairs * args.steps / (total_ms * 1e-3)
-    tops = ops * args.steps / (total_ms * 1e-3) / 1e12
+    value = world * n_pairs * args.steps / (total_ms * 1e-3)
+    tops = world * ops * args.steps / (total_ms * 1e-3) / 1e12
     peak_tflops, _, peak_kind = _peaks()
     line = {"metric": "image pairs/sec (batch), int8-equivalent TOPS", "value": value, "unit": UNIT,
-            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "config": {"workload": desc, "pairs": n_pairs,
                                              "l2": "flushed before every step (256 MiB write)",
-                                             "graph": "one CUDA graph per step (match_batch), replayed"},
+                                             "graph": "one CUDA graph per step (match_batch), replayed",
+                                             "parallelism": f"replicas x{world}"},
             "int8_equiv_tops": tops,
             "roofline": {"bound": "tensor", "achieved": tops, "peak": peak_tflops, "unit": "TFLOP/s",
-                         "frac": tops / peak_tflops, "traffic": None,
+                         "frac": tops / world / peak_tflops, "traffic": None,
                          "kernel": "whole step (all launches of match_batch)",
                          "peak_kind": f"bf16 dense burst, {peak_kind}"},
             "e2e": None, "gpu_launches": launches * args.steps, "clocks": clk}
@@ -486,15 +494,15 @@ def run_batch(args):
         if st >= 3:
             e2e_evs.append((e0, e1))
     stream.synchronize()
-    e2e_ms = sum(e0.elapsed_time(e1) for e0, e1 in e2e_evs)
+    e2e_ms = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in e2e_evs), dev)
     same = all(torch.equal(o.result(), h.result()) for o, h in zip(outs, e2e_outs))
-    line["e2e"] = {"value": n_pairs * e2e_steps / (e2e_ms * 1e-3), "unit": UNIT,
+    line["e2e"] = {"value": world * n_pairs * e2e_steps / (e2e_ms * 1e-3), "unit": UNIT,
                    "h2d_bytes_per_step": sum(x.shape[0] * 128 for x in imgs_np),
                    "d2h_bytes_per_step": sum(4 + 8 * int(h.count.item()) for h in e2e_outs),
                    "steps": e2e_steps, "equals_device_resident_result": bool(same),
                    "path": "match_batch on pinned host images, outputs in pinned host memory "
                            "(kernels read and write the host directly)"}
-    if not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build_library()
         rng = np.random.default_rng(0)
@@ -514,7 +522,10 @@ def run_batch(args):
         line["cpu_baseline"] = {"value": n_done / dt * (done_ops / n_done) / (ops / n_pairs), "unit": UNIT,
                                 "cores": oracle.max_threads(), "kind": "oracle",
                                 "sample": f"{n_done} pairs in {dt:.1f} s, scaled to the workload's mean pair"}
-    print(json.dumps(line), flush=True)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
     return 0
 
 

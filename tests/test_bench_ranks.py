@@ -56,3 +56,53 @@ def test_reference_arm_non_zero_rank_exits_quietly():
                         "--steps", "3", "--warmup", "3"], env=env, capture_output=True, text=True,
                        timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def _shard_worker(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+
+    import sift_synth
+    import top_ratio_test_gb300 as serac
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    sizes = [tuple(int(v) for v in x) for x in sift_synth.ragged_sizes(0)]
+    mine = serac.shard_pairs(sizes, world)[rank]
+    # every rank computes the same partition; gather what each rank takes
+    got = [None] * world
+    dist.all_gather_object(got, mine)
+    load = torch.tensor([float(sum(sizes[k][0] * sizes[k][1] for k in mine))])
+    loads = [torch.zeros(1) for _ in range(world)]
+    dist.all_gather(loads, load)
+    q.put((rank, got, [float(x) for x in loads]))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_shard_pairs_gloo():
+    """The 256-pair ragged batch split over two gloo ranks: the ranks agree on the
+    partition, every pair goes to exactly one rank, and the costs are balanced."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_shard_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = dict((r, (g, l)) for r, g, l in (q.get() for _ in range(2)))
+    assert res[0][0] == res[1][0]
+    shards = res[0][0]
+    assert sorted(shards[0] + shards[1]) == list(range(256))
+    loads = res[0][1]
+    assert max(loads) / (sum(loads) / 2) < 1.01
+
+
+def test_shard_pairs_edge_cases():
+    sys.path.insert(0, ROOT)
+    import top_ratio_test_gb300 as serac
+    assert serac.shard_pairs([], 3) == [[], [], []]
+    assert serac.shard_pairs([(5, 5)], 1) == [[0]]
+    assert serac.shard_pairs([(10, 10), (1, 1), (10, 10)], 2) == [[0, 1], [2]]

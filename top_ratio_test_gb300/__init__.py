@@ -299,6 +299,24 @@ def scores(a: torch.Tensor, b: torch.Tensor, *, workspace_t: Optional[torch.Tens
     return out[:n_a, :n_b]
 
 
+def shard_pairs(sizes: Sequence, world: int) -> list:
+    """Split pairs with these (n_a, n_b) over `world` GPUs, one process each, by cost
+    (n_a * n_b, the contraction's size): longest-processing-time greedy, each pair to
+    the least-loaded rank.  Returns, per rank, the ascending indices of its pairs.
+    Pairs are independent, so a rank runs match_batch on its own shard and no data
+    crosses ranks; a caller that wants every result in one place gathers them after."""
+    if world < 1:
+        raise ValueError("world must be >= 1")
+    order = sorted(range(len(sizes)), key=lambda k: (-int(sizes[k][0]) * int(sizes[k][1]), k))
+    load = [0] * world
+    shards = [[] for _ in range(world)]
+    for k in order:
+        r = min(range(world), key=lambda i: (load[i], i))
+        shards[r].append(k)
+        load[r] += int(sizes[k][0]) * int(sizes[k][1])
+    return [sorted(x) for x in shards]
+
+
 def schedule_describe(sizes: Sequence, grid: int):
     """Host-side view of how the first launch chunk of pairs with these (n_a, n_b)
     sizes is cut: (chunks, items, nsplit per pair, cta_first[grid + 1])."""
