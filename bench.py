@@ -255,7 +255,12 @@ def run_ours(args):
     if st != serac.OK:
         raise SystemExit(f"device check failed: {serac.status_str(st)}")
 
-    pair = sift_synth.single_pair_8192(0) if args.workload == "pair8192" else sift_synth.single_pair_2000(0)
+    if args.n:
+        pair = sift_synth.make_pair(0, 1, args.n, args.n, args.n, 0.25, 0.08)
+    elif args.workload == "pair8192":
+        pair = sift_synth.single_pair_8192(0)
+    else:
+        pair = sift_synth.single_pair_2000(0)
     n_a, n_b = pair.a.shape[0], pair.b.shape[0]
     ops_per_pair = 2 * n_a * n_b * 128
     a_host = torch.from_numpy(pair.a).pin_memory()
@@ -356,14 +361,16 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD if args.workload == "pair8192" else WORKLOAD_2000, "n_a": n_a, "n_b": n_b,
+        "config": {"workload": (f"single pair {n_a}x{n_b} SIFT-shaped u8 descriptors, 25% planted at sigma 0.08, "
+                                f"seed 0" if args.n else WORKLOAD if args.workload == "pair8192" else WORKLOAD_2000),
+                   "n_a": n_a, "n_b": n_b,
                    "l2": "flushed before every step (256 MiB write)",
                    "graph": "one CUDA graph per step, replayed; kernels chained by programmatic dependent launch",
                    "parallelism": f"replicas x{world}"},
         "int8_equiv_tops": value * ops_per_pair / 1e12,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved / peak_tflops,
-                     "traffic": FUSED_TRAFFIC_8192 if args.workload == "pair8192" else None,
+                     "traffic": FUSED_TRAFFIC_8192 if args.workload == "pair8192" and not args.n else None,
                      "kernel": "fused_top2_kernel", "peak_kind": f"bf16 dense burst, {peak_kind}",
                      "fused_ms": fused_ms, "timing": "fused-kernel events in a second timed pass of the "
                      "same steps (event nodes in the step graph would serialise its launches)",
@@ -539,12 +546,14 @@ def main():
     ap.add_argument("--workload", choices=["pair8192", "pair2000", "ring12", "ragged256", "survey100"],
                     default="pair8192", help="pair8192 is the headline; the others are batch lines "
                     "for the tables (match_batch over the whole workload per step)")
+    ap.add_argument("--n", type=int, default=0,
+                    help="a single n x n pair (same recipe as the 8192 x 8192 one) instead of the workload")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
-    if args.workload in ("pair8192", "pair2000"):
+    if args.n or args.workload in ("pair8192", "pair2000"):
         return run_ours(args)
     return run_batch(args)
 
