@@ -185,13 +185,15 @@ int match_pair_noalloc(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b
                        const serac_params* params, const serac_out* out, void* cuda_stream);
 
 /* Host-only view of the work schedule (no GPU needed): for `pairs` (pointers are
- * used only to recognise shared images) and a persistent grid of `grid` CTAs
- * (1..256), report the number of launch chunks, and for the first chunk the number
- * of work items, the column splits per pair (out_nsplit[n_pairs of that chunk]) and
- * the item ranges cta_first[grid + 1] (CTA c takes items [cta_first[c],
- * cta_first[c+1])).  Any output may be NULL.  Returns SERAC_EINVAL on bad input. */
+ * used only to recognise shared images) and at most `grid` persistent CTAs
+ * (1..256), report the number of launch chunks and, for the first chunk, the total
+ * number of pieces, the pieces of each pair (out_npieces[pairs of that chunk]; a
+ * pair's 128 x 256 tiles are cut into that many runs, one per CTA, 0 for an empty
+ * pair) and the tiles each CTA processes (cta_tiles[grid]; CTAs beyond the chunk's
+ * launch grid, which has at most one CTA per tile, get 0).  Any output may be NULL.
+ * Returns SERAC_EINVAL on bad input. */
 int serac_schedule_describe(const serac_pair* pairs, int32_t n_pairs, int32_t grid, int32_t* out_chunks,
-                            int32_t* out_items, int32_t* out_nsplit, int32_t* cta_first);
+                            int32_t* out_pieces, int32_t* out_npieces, int32_t* cta_tiles);
 
 /* Static text for a status code. */
 const char* serac_status_str(int status);

@@ -90,38 +90,55 @@ def test_bad_arguments_rejected_before_any_launch(serac):
     assert L.match_batch(None, -1, ctypes.byref(p), None, 256, ws, None) == serac.EINVAL
 
 
+def _tiles(na, nb):
+    return ((na + 127) // 128) * ((nb + 255) // 256) if na > 0 and nb > 0 else 0
+
+
 def test_schedule_covers_every_tile_once(serac):
-    # a single 8192 x 8192 pair on 152 CTAs
-    chunks, items, nsplit, first = serac.schedule_describe([(8192, 8192)], 152)
+    # a single 8192 x 8192 pair on 152 CTAs: 2048 tiles dealt 13 or 14 per CTA
+    chunks, pieces, npieces, cta = serac.schedule_describe([(8192, 8192)], 152)
     assert chunks == 1
-    assert nsplit == [19] and items == 64 * 19
-    assert first[0] == 0 and first[-1] == items
-    assert all(first[c] <= first[c + 1] for c in range(152))
-    # items go to the CTA holding their midpoint: loads differ by at most one tile here
-    cts = 32
-    per_item = [(s + 1) * cts // 19 - s * cts // 19 for s in range(19)] * 64
-    loads = [sum(per_item[first[c]:first[c + 1]]) for c in range(152)]
-    assert sum(loads) == 64 * 32
-    assert max(loads) - min(loads) <= 1
+    assert npieces == [152] and pieces == 152
+    assert sum(cta) == 64 * 32
+    assert sorted(set(cta)) == [13, 14] and cta.count(14) == 2048 % 152
+
+
+def test_schedule_small_pair_uses_fewer_ctas(serac):
+    # 2000 x 2000: 16 x 8 = 128 tiles, one per CTA; the other 24 CTAs are not launched
+    chunks, pieces, npieces, cta = serac.schedule_describe([(2000, 2000)], 152)
+    assert npieces == [128] and pieces == 128
+    assert cta[:128] == [1] * 128 and cta[128:] == [0] * 24
 
 
 def test_schedule_ragged_and_empty(serac):
     sizes = [(1000, 16384), (0, 500), (257, 0), (129, 255), (16384, 1000)]
-    chunks, items, nsplit, first = serac.schedule_describe(sizes, 152)
-    assert nsplit[1] == 0 and nsplit[2] == 0
-    rt = [(na + 127) // 128 for na, _ in sizes]
-    ct = [(nb + 255) // 256 for _, nb in sizes]
-    assert all(1 <= nsplit[k] <= ct[k] for k in (0, 3, 4))
-    assert items == sum(rt[k] * nsplit[k] for k in range(5))
-    assert first[-1] == items and first[0] == 0
+    chunks, pieces, npieces, cta = serac.schedule_describe(sizes, 152)
+    t = [_tiles(na, nb) for na, nb in sizes]
+    assert npieces == [min(152, x) for x in t]
+    assert npieces[1] == 0 and npieces[2] == 0
+    assert pieces == sum(npieces)
+    assert sum(cta) == sum(t)
+    # tiles are dealt round-robin across pairs: loads differ by at most one
+    assert max(cta) - min(cta) <= 1
+
+
+def test_schedule_balanced_over_many_pairs(serac):
+    # 40 pairs of 1,700 tiles and 40 of 5 tiles: every CTA within one tile of the mean
+    sizes = [(6400, 8704), (640, 256)] * 40
+    chunks, pieces, npieces, cta = serac.schedule_describe(sizes, 152)
+    assert chunks == 1
+    total = sum(_tiles(na, nb) for na, nb in sizes)
+    assert sum(cta) == total
+    assert max(cta) - min(cta) <= 1
 
 
 def test_schedule_large_batch_chunks(serac):
     sizes = [(8192, 8192)] * 300
-    chunks, items, nsplit, first = serac.schedule_describe(sizes, 152)
+    chunks, pieces, npieces, cta = serac.schedule_describe(sizes, 152)
     # at most 128 pairs per launch chunk (their tables travel as kernel parameters)
     assert chunks == 3
-    assert nsplit[0] == 1 and items == 128 * 64
+    assert npieces[0] == 152 and pieces == 128 * 152
+    assert sum(cta) == 128 * 2048 and max(cta) - min(cta) <= 1
 
 
 def test_timeout_hook_is_host_only(serac):

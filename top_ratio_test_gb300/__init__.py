@@ -319,14 +319,14 @@ def shard_pairs(sizes: Sequence, world: int) -> list:
 
 def schedule_describe(sizes: Sequence, grid: int):
     """Host-side view of how the first launch chunk of pairs with these (n_a, n_b)
-    sizes is cut: (chunks, items, nsplit per pair, cta_first[grid + 1])."""
+    sizes is cut: (chunks, pieces, pieces per pair, tiles per CTA[grid])."""
     n = len(sizes)
     arr = (_Pair * max(n, 1))()
     for k, (na, nb) in enumerate(sizes):
         arr[k] = _Pair(16 * (2 * k + 1), int(na), 16 * (2 * k + 2), int(nb))
-    chunks, items = ctypes.c_int32(), ctypes.c_int32()
-    nsplit = (ctypes.c_int32 * max(n, 1))()
-    first = (ctypes.c_int32 * (grid + 1))()
-    _check(lib().serac_schedule_describe(arr, n, grid, ctypes.byref(chunks), ctypes.byref(items),
-                                         nsplit, first), "serac_schedule_describe")
-    return chunks.value, items.value, list(nsplit)[:n], list(first)
+    chunks, pieces = ctypes.c_int32(), ctypes.c_int32()
+    npieces = (ctypes.c_int32 * max(n, 1))()
+    cta_tiles = (ctypes.c_int32 * grid)()
+    _check(lib().serac_schedule_describe(arr, n, grid, ctypes.byref(chunks), ctypes.byref(pieces),
+                                         npieces, cta_tiles), "serac_schedule_describe")
+    return chunks.value, pieces.value, list(npieces)[:n], list(cta_tiles)

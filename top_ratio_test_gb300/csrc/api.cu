@@ -3,10 +3,11 @@
 //
 // Schedule.  Pairs are processed in launch chunks of at most MAX_PAIRS pairs (the
 // per-pair tables travel as kernel parameters, so a call needs no host-to-device
-// copy and can be captured in a CUDA graph).  Within a chunk every pair is cut into
-// work items (row tile x column split); the split count is chosen so the chunk has
-// at least ~8 items per SM of a 152-SM GB300, and items are handed to the
-// persistent CTAs as contiguous ranges of equal tile count.
+// copy and can be captured in a CUDA graph).  Within a chunk every pair's tiles are
+// cut into as many pieces as there are persistent CTAs (fewer for small pairs), one
+// piece per CTA, with the CTA of a pair's first piece rotating from pair to pair so
+// that the CTAs' tile counts stay within one tile per pair of each other; every CTA
+// walks the pairs in the same order, so the pairs in flight share L2.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -23,8 +24,6 @@
 namespace serac {
 namespace {
 
-constexpr int TARGET_CTAS = 152;            // SMs of a GB300; fixes the item cut
-constexpr int ITEMS_PER_CTA = 8;
 constexpr int64_t CHUNK_KEY_BYTES = 64ll << 20;
 constexpr size_t ALIGN = 1024;
 
@@ -32,8 +31,7 @@ size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 
 struct Chunk {
   int p0 = 0, p1 = 0;          // pairs [p0, p1)
-  int nsplit_target = 1;
-  int64_t items = 0;
+  int64_t tiles = 0;           // 128 x 256 tiles of all its pairs
   int64_t rows = 0, cols = 0;  // sum of n_a, n_b
   int64_t blocks = 0;          // match-kernel blocks
 };
@@ -54,9 +52,9 @@ int64_t col_tiles(int32_t n_b) { return (static_cast<int64_t>(n_b) + BN - 1) / B
 
 int64_t match_blocks(int32_t n_a) { return std::max<int64_t>(1, (static_cast<int64_t>(n_a) + MATCH_ROWS_PER_BLOCK - 1) / MATCH_ROWS_PER_BLOCK); }
 
-int pair_nsplit(const serac_pair& pr, int target) {
+int64_t pair_tiles(const serac_pair& pr) {
   if (pr.n_a <= 0 || pr.n_b <= 0) return 0;
-  return static_cast<int>(std::min<int64_t>(target, col_tiles(pr.n_b)));
+  return row_tiles(pr.n_a) * col_tiles(pr.n_b);
 }
 
 void build_plan(const serac_pair* pairs, int32_t n_pairs, Plan& pl) {
@@ -95,15 +93,8 @@ void build_plan(const serac_pair* pairs, int32_t n_pairs, Plan& pl) {
       ++p;
     }
     ch.p1 = p;
-    int64_t rtt = 0;
-    for (int k = ch.p0; k < ch.p1; ++k)
-      if (pairs[k].n_a > 0 && pairs[k].n_b > 0) rtt += row_tiles(pairs[k].n_a);
-    ch.nsplit_target = rtt > 0 ? static_cast<int>(std::max<int64_t>(
-                                     1, (static_cast<int64_t>(ITEMS_PER_CTA) * TARGET_CTAS + rtt - 1) / rtt))
-                               : 1;
     for (int k = ch.p0; k < ch.p1; ++k) {
-      const int ns = pair_nsplit(pairs[k], ch.nsplit_target);
-      ch.items += row_tiles(pairs[k].n_a) * ns;
+      ch.tiles += pair_tiles(pairs[k]);
       ch.rows += pairs[k].n_a;
       ch.cols += pairs[k].n_b;
       ch.blocks += match_blocks(pairs[k].n_a);
@@ -138,32 +129,26 @@ void build_plan(const serac_pair* pairs, int32_t n_pairs, Plan& pl) {
   pl.total = off;
 }
 
-// Contiguous item ranges of equal tile count: item i, covering tiles
-// [Q_i, Q_i + w_i) of C, goes to the CTA its midpoint falls in,
-// floor((2 Q_i + w_i) * G / 2C).
-void cut_items(const serac_pair* pairs, const Chunk& ch, int grid, int32_t* cta_first) {
-  const int64_t total_items = ch.items;
-  int64_t total_cost = 0;
-  for (int k = ch.p0; k < ch.p1; ++k)
-    if (pair_nsplit(pairs[k], ch.nsplit_target) > 0) total_cost += row_tiles(pairs[k].n_a) * col_tiles(pairs[k].n_b);
-  for (int c = 0; c <= grid; ++c) cta_first[c] = static_cast<int32_t>(total_items);
-  int64_t item = 0, q = 0;
-  int next_cta = 0;
+// CTAs of a chunk's launch: one per SM, at most one per tile.
+int chunk_grid(const Chunk& ch, int sms) {
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({static_cast<int64_t>(sms), ch.tiles, MAX_GRID})));
+}
+
+// Tiles of piece k when T tiles are dealt to `grid` CTAs: T / grid each, and one
+// more for the first T mod grid pieces.
+int64_t piece_tiles(int64_t t, int grid, int k) { return t / grid + (k < t % grid ? 1 : 0); }
+
+// Pieces per pair (min(grid, tiles)) and the CTA of each pair's first piece.  The
+// pieces that carry one tile more go to the CTAs after those that took the previous
+// pair's, so over a chunk every CTA gets the same number of tiles within one.
+void plan_pieces(const serac_pair* pairs, const Chunk& ch, int grid, int32_t* npieces, int32_t* offset) {
+  int off = 0;
   for (int k = ch.p0; k < ch.p1; ++k) {
-    const int ns = pair_nsplit(pairs[k], ch.nsplit_target);
-    if (ns == 0) continue;
-    const int64_t rts = row_tiles(pairs[k].n_a), cts = col_tiles(pairs[k].n_b);
-    for (int64_t rt = 0; rt < rts; ++rt) {
-      for (int s = 0; s < ns; ++s, ++item) {
-        const int64_t w = (s + 1) * cts / ns - s * cts / ns;
-        int c = static_cast<int>(total_cost > 0 ? (2 * q + w) * grid / (2 * total_cost) : 0);
-        if (c > grid - 1) c = grid - 1;
-        while (next_cta <= c) cta_first[next_cta++] = static_cast<int32_t>(item);
-        q += w;
-      }
-    }
+    const int64_t t = pair_tiles(pairs[k]);
+    npieces[k - ch.p0] = static_cast<int>(std::min<int64_t>(grid, t));
+    offset[k - ch.p0] = off;
+    off = static_cast<int>((off + t % grid) % grid);
   }
-  while (next_cta <= grid) cta_first[next_cta++] = static_cast<int32_t>(total_items);
 }
 
 // ------------------------------------------------------------------ device state
@@ -324,11 +309,12 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
     unsigned long long* rowkeys = reinterpret_cast<unsigned long long*>(region + pl.r_rowkeys);
     unsigned long long* colkeys = reinterpret_cast<unsigned long long*>(region + pl.r_colkeys);
     // ---------------- fused GEMM + top-2, merged into the key arrays
-    if (ch.items > 0) {
+    if (ch.tiles > 0) {
       FusedParams fp;
       std::memset(&fp, 0, sizeof(fp));
-      fp.grid = static_cast<int32_t>(std::min<int64_t>({static_cast<int64_t>(sms), ch.items, MAX_GRID}));
-      fp.n_items = static_cast<int32_t>(ch.items);
+      fp.grid = chunk_grid(ch, sms);
+      int32_t npieces[MAX_PAIRS], offset[MAX_PAIRS];
+      plan_pieces(pairs, ch, fp.grid, npieces, offset);
       fp.rowkeys = rowkeys;
       fp.colkeys = colkeys;
       fp.err = err;
@@ -338,26 +324,23 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
       fp.no_copies = (first_fused && g_inject_no_copies) ? 1 : 0;
       if (first_fused) g_inject_no_copies = false;
       int np = 0;
-      int64_t item_base = 0, rows = 0, cols = 0;
+      int64_t rows = 0, cols = 0;
       for (int k = ch.p0; k < ch.p1; ++k) {
-        const int ns = pair_nsplit(pairs[k], ch.nsplit_target);
-        if (ns > 0) {
+        if (npieces[k - ch.p0] > 0) {
           FusedPair& f = fp.pairs[np++];
           f.a_row0 = pl.images[pl.a_img[k]].row0;
           f.b_row0 = pl.images[pl.b_img[k]].row0;
           f.n_a = pairs[k].n_a;
           f.n_b = pairs[k].n_b;
-          f.nsplit = ns;
-          f.item_base = static_cast<int32_t>(item_base);
+          f.npieces = npieces[k - ch.p0];
+          f.offset = offset[k - ch.p0];
           f.row_base = static_cast<int32_t>(rows);
           f.col_base = static_cast<int32_t>(cols);
-          item_base += row_tiles(pairs[k].n_a) * ns;
         }
         rows += pairs[k].n_a;
         cols += pairs[k].n_b;
       }
       fp.n_pairs = np;
-      cut_items(pairs, ch, fp.grid, fp.cta_first);
       const bool prof = first_fused && g_ev_begin && g_ev_end;
       if (prof)
         SERAC_TRY_CUDA(cudaEventRecordWithFlags(g_ev_begin, static_cast<cudaStream_t>(stream), cudaEventRecordExternal));
@@ -529,16 +512,28 @@ int serac_last_launch_count(void) { return g_last_launches; }
 int serac_last_cuda_error(void) { return g_last_cuda_error; }
 
 int serac_schedule_describe(const serac_pair* pairs, int32_t n_pairs, int32_t grid, int32_t* out_chunks,
-                            int32_t* out_items, int32_t* out_nsplit, int32_t* cta_first) {
+                            int32_t* out_pieces, int32_t* out_npieces, int32_t* cta_tiles) {
   if (check_pairs(pairs, n_pairs) != SERAC_OK || grid <= 0 || grid > MAX_GRID) return SERAC_EINVAL;
   Plan pl;
   build_plan(pairs, n_pairs, pl);
   if (out_chunks) *out_chunks = static_cast<int32_t>(pl.chunks.size());
   const Chunk& ch = pl.chunks.front();
-  if (out_items) *out_items = static_cast<int32_t>(ch.items);
-  if (out_nsplit)
-    for (int k = ch.p0; k < ch.p1; ++k) out_nsplit[k - ch.p0] = pair_nsplit(pairs[k], ch.nsplit_target);
-  if (cta_first) cut_items(pairs, ch, grid, cta_first);
+  const int g = chunk_grid(ch, grid);
+  int32_t npieces[MAX_PAIRS], offset[MAX_PAIRS];
+  plan_pieces(pairs, ch, g, npieces, offset);
+  int64_t total = 0;
+  for (int k = ch.p0; k < ch.p1; ++k) total += npieces[k - ch.p0];
+  if (out_pieces) *out_pieces = static_cast<int32_t>(total);
+  if (out_npieces)
+    for (int k = ch.p0; k < ch.p1; ++k) out_npieces[k - ch.p0] = npieces[k - ch.p0];
+  if (cta_tiles) {
+    for (int c = 0; c < grid; ++c) cta_tiles[c] = 0;
+    for (int k = ch.p0; k < ch.p1; ++k) {
+      const int64_t t = pair_tiles(pairs[k]);
+      for (int i = 0; i < npieces[k - ch.p0]; ++i)
+        cta_tiles[(offset[k - ch.p0] + i) % g] += static_cast<int32_t>(piece_tiles(t, g, i));
+    }
+  }
   return SERAC_OK;
 }
 

@@ -81,38 +81,40 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
-struct Item {
+// Where a CTA stands in its work: pair p, the next tile t of its piece of that pair
+// and the piece's end (tiles numbered row-major within the pair).
+struct Cursor {
+  int p, t, tend;
+};
+
+// One segment: row tile rt of pair p against the column tiles [ct0, ct1).
+struct Segment {
   int p, rt, ct0, ct1;
 };
 
-__device__ __forceinline__ Item decode_item(const FusedParams& P, int item) {
-  int lo = 0, hi = P.n_pairs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (P.pairs[mid].item_base <= item) lo = mid; else hi = mid - 1;
+// Advances `cur` by one segment; false once the CTA has no work left.  Piece k of a
+// pair belongs to CTA (offset + k) mod grid: the pair's T tiles are dealt as q = T / grid
+// tiles per piece plus one more for the first r = T mod grid pieces, so piece k starts
+// at tile k q + min(k, r).
+__device__ __forceinline__ bool next_segment(const FusedParams& P, Cursor& cur, Segment& g) {
+  while (cur.t >= cur.tend) {
+    if (++cur.p >= P.n_pairs) return false;
+    const FusedPair& fp = P.pairs[cur.p];
+    int k = static_cast<int>(blockIdx.x) - fp.offset;
+    if (k < 0) k += P.grid;
+    if (k >= fp.npieces) continue;
+    const int tiles = ((fp.n_a + BM - 1) / BM) * ((fp.n_b + BN - 1) / BN);
+    const int q = tiles / P.grid, r = tiles - q * P.grid;
+    cur.t = k * q + min(k, r);
+    cur.tend = cur.t + q + (k < r ? 1 : 0);
   }
-  const FusedPair& fp = P.pairs[lo];
-  const int local = item - fp.item_base;
-  const int rt = local / fp.nsplit, s = local - rt * fp.nsplit;
-  const int ct_total = (fp.n_b + BN - 1) / BN;
-  return Item{lo, rt, s * ct_total / fp.nsplit, (s + 1) * ct_total / fp.nsplit};
-}
-
-// The segment starting at item `it`: the run of items [it, next) on one row tile.
-struct Segment {
-  Item s;
-  int next;
-};
-
-__device__ __forceinline__ Segment next_segment(const FusedParams& P, int it, int it1) {
-  Segment g{decode_item(P, it), it + 1};
-  while (g.next < it1) {
-    const Item J = decode_item(P, g.next);
-    if (J.p != g.s.p || J.rt != g.s.rt) break;
-    g.s.ct1 = J.ct1;
-    ++g.next;
-  }
-  return g;
+  const int ct_total = (P.pairs[cur.p].n_b + BN - 1) / BN;
+  g.p = cur.p;
+  g.rt = cur.t / ct_total;
+  g.ct0 = cur.t - g.rt * ct_total;
+  g.ct1 = min(ct_total, g.ct0 + (cur.tend - cur.t));
+  cur.t += g.ct1 - g.ct0;
+  return true;
 }
 
 // ---- key arithmetic
@@ -238,8 +240,6 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
   // the staged operands, the cleared keys and the error word are read after this
   grid_dep_wait();
 
-  const int it0 = P.cta_first[blockIdx.x], it1 = P.cta_first[blockIdx.x + 1];
-
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     // (no_copies: the failure-detection test hook -- nothing is loaded, so the MMA's
@@ -247,16 +247,16 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     if (lane == 0 && !P.no_copies) {
       uint32_t bcount = 0, nseg = 0;
       bool ok = true;
-      for (int it = it0; it < it1 && ok; ++nseg) {
-        const Segment g = next_segment(P, it, it1);
-        it = g.next;
-        const FusedPair& fp = P.pairs[g.s.p];
+      Cursor cur{-1, 0, 0};
+      Segment g;
+      for (; ok && next_segment(P, cur, g); ++nseg) {
+        const FusedPair& fp = P.pairs[g.p];
         if (!mbar_wait(a_empty, (nseg & 1u) ^ 1u, abort_flag, P.err, ERR_TIMEOUT_PRODUCER, WAIT_LIMIT_NS)) break;
         mbar_arrive_expect_tx(a_full, A_BYTES);
-        const int ay = fp.a_row0 + g.s.rt * BM;
+        const int ay = fp.a_row0 + g.rt * BM;
         tma_load_2d(sA, &tmap, a_full, 0, ay);
         tma_load_2d(sA + A_HALF, &tmap, a_full, 64, ay);
-        for (int ct = g.s.ct0; ct < g.s.ct1; ++ct, ++bcount) {
+        for (int ct = g.ct0; ct < g.ct1; ++ct, ++bcount) {
           const uint32_t st = bcount & 1u, ph = (bcount >> 1) & 1u;
           if (!mbar_wait(&b_empty[st], ph ^ 1u, abort_flag, P.err, ERR_TIMEOUT_PRODUCER, WAIT_LIMIT_NS)) {
             ok = false;
@@ -287,12 +287,12 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
       const uint64_t a_bias = plain_kmajor_desc(bias_addr, 128, 0);
       const uint64_t b_bias = plain_kmajor_desc(bias_addr + 256, 128, 0);
       bool ok = true;
-      for (int it = it0; it < it1 && ok; ++nseg) {
-        const Segment g = next_segment(P, it, it1);
-        it = g.next;
+      Cursor cur{-1, 0, 0};
+      Segment g;
+      for (; ok && next_segment(P, cur, g); ++nseg) {
         if (!mbar_wait(a_full, nseg & 1u, abort_flag, P.err, ERR_TIMEOUT_MMA, WAIT_LIMIT_NS)) break;
         tc_fence_after();
-        for (int ct = g.s.ct0; ct < g.s.ct1; ++ct, ++bcount, ++tcount) {
+        for (int ct = g.ct0; ct < g.ct1; ++ct, ++bcount, ++tcount) {
           const uint32_t st = bcount & 1u, ph = (bcount >> 1) & 1u;
           const uint32_t acc = tcount & 1u, aph = (tcount >> 1) & 1u;
           if (!mbar_wait(&b_full[st], ph, abort_flag, P.err, ERR_TIMEOUT_MMA, WAIT_LIMIT_NS) ||
@@ -346,13 +346,16 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     // returning atomic's latency overlaps the next tile
     unsigned long long* pend_ptr = nullptr;
     unsigned long long pend_old = 0ull, pend_x1 = 0ull;
-    for (int it = it0; it < it1;) {
-      const Segment g = next_segment(P, it, it1);
-      it = g.next;
-      const FusedPair& fp = P.pairs[g.s.p];
+    // the same for the row's second slot, deferred to the end of the next segment
+    unsigned long long* rpend_ptr = nullptr;
+    unsigned long long rpend_old = 0ull, rpend_k1 = 0ull;
+    Cursor cur{-1, 0, 0};
+    Segment g;
+    while (next_segment(P, cur, g)) {
+      const FusedPair& fp = P.pairs[g.p];
       unsigned long long K1 = 0ull, K2 = 0ull;  // the row's top-2 over the segment
       uint32_t thr = 0;                          // tile keys below this cannot enter
-      for (int ct = g.s.ct0; ct < g.s.ct1; ++ct, ++tcount) {
+      for (int ct = g.ct0; ct < g.ct1; ++ct, ++tcount) {
         const uint32_t acc = tcount & 1u, aph = (tcount >> 1) & 1u;
         // on a timeout keep going (results are flagged invalid): every epilogue warp
         // must pass the same named-barrier sequence
@@ -367,7 +370,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
           tmem_ld_32x32b_x16(taddr + c * 16, v);
           tmem_wait_ld();
           if constexpr (DUMP) {
-            const int row = g.s.rt * BM + static_cast<int>(rl);
+            const int row = g.rt * BM + static_cast<int>(rl);
             if (row < fp.n_a) {
 #pragma unroll
               for (int k = 0; k < 16; ++k) {
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
             }
             const int j = ct * BN + col;
             if (j < fp.n_b) {
-              const uint32_t rbase = static_cast<uint32_t>(g.s.rt * BM);
+              const uint32_t rbase = static_cast<uint32_t>(g.rt * BM);
               const unsigned long long x1 = key64(__float_as_uint(m1), rbase);
               const unsigned long long x2 = key64(__float_as_uint(m2), rbase);
               if (x1) {
@@ -456,12 +459,17 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
         }
       }
       if constexpr (!DUMP) {
-        const int i = g.s.rt * BM + static_cast<int>(rl);
+        if (rpend_ptr) {
+          const unsigned long long lo = rpend_old < rpend_k1 ? rpend_old : rpend_k1;
+          if (lo) atomicMax(rpend_ptr, lo);
+          rpend_ptr = nullptr;
+        }
+        const int i = g.rt * BM + static_cast<int>(rl);
         if (ok && i < fp.n_a && K1) {
           unsigned long long* rk = P.rowkeys + 2 * static_cast<int64_t>(fp.row_base + i);
-          const unsigned long long old = atomicMax(rk, K1);
-          const unsigned long long lo = old < K1 ? old : K1;
-          if (lo) atomicMax(rk + 1, lo);
+          rpend_old = atomicMax(rk, K1);
+          rpend_k1 = K1;
+          rpend_ptr = rk + 1;
           if (K2) atomicMax(rk + 1, K2);
         }
       }
@@ -469,6 +477,10 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     if (pend_ptr) {
       const unsigned long long lo = pend_old < pend_x1 ? pend_old : pend_x1;
       if (lo) atomicMax(pend_ptr, lo);
+    }
+    if (rpend_ptr) {
+      const unsigned long long lo = rpend_old < rpend_k1 ? rpend_old : rpend_k1;
+      if (lo) atomicMax(rpend_ptr, lo);
     }
   }
 

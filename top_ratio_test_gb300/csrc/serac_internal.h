@@ -6,11 +6,14 @@
 // one buffer that a single TMA tensor map covers; the zero rows score 0 and the
 // zero floor drops them, so ragged tails need no masking.
 //
-// Work item = (pair, row tile, column split).  Items are cut so that every launch
-// has at least a few items per SM; each CTA of the persistent fused kernel takes a
-// contiguous range of items balanced by tile count, and runs of its items on the
-// same row tile form one segment: one A tile resident in shared memory against a
-// contiguous run of B tiles, with one running row top-2.
+// Work: in a launch chunk, every CTA of the persistent fused kernel takes one piece
+// of every pair (piece k of pair p goes to CTA (offset_p + k) mod grid; a pair's T
+// tiles are dealt T / grid per piece, one more for the first T mod grid pieces, and
+// a pair with fewer tiles than CTAs has one-tile pieces).  A piece is a run of the pair's tiles in
+// row-major order, processed as segments: one A tile resident in shared memory
+// against a run of B tiles of one row tile, with one running row top-2.  All CTAs thus
+// work through the pairs in the same order, so the operands of the pairs in flight
+// stay in L2, and every CTA gets the same number of tiles within one per pair.
 #pragma once
 #include <stdint.h>
 
@@ -36,8 +39,8 @@ struct FusedPair {
   int32_t a_row0;      // first staged row of image A
   int32_t b_row0;      // first staged row of image B
   int32_t n_a, n_b;
-  int32_t nsplit;      // column splits per row tile (<= column tiles)
-  int32_t item_base;   // first work item of this pair
+  int32_t npieces;     // pieces the pair's tiles are cut into (<= grid)
+  int32_t offset;      // piece k goes to CTA (offset + k) mod grid
   int32_t row_base;    // first row-key entry of this pair
   int32_t col_base;    // first column-key entry of this pair
 };
@@ -47,7 +50,6 @@ struct FusedPair {
 // by score, then lower index.  Kernels merge into them with atomicMax.
 struct FusedParams {
   int32_t n_pairs;
-  int32_t n_items;
   int32_t grid;
   int32_t dump_ld;                   // score-dump row stride (dump mode only)
   unsigned long long* rowkeys;       // [rows of the chunk][2]
@@ -56,7 +58,6 @@ struct FusedParams {
   int32_t* dump;                     // score dump (dump mode only)
   uint32_t key_mult;                 // 256, read as a kernel parameter (see the epilogue)
   int32_t no_copies;                 // test hook: the producer issues no copies (bounded waits run out)
-  int32_t cta_first[MAX_GRID + 1];   // items [cta_first[c], cta_first[c+1]) go to CTA c
   FusedPair pairs[MAX_PAIRS];
 };
 
