@@ -151,6 +151,26 @@ def test_batch_many_images_and_chunks(serac, oracle_mod):
         np.testing.assert_array_equal(outs[k].result().numpy(), ref.matches)
 
 
+def test_batch_mixed_piece_sizes(serac, oracle_mod):
+    """One launch chunk whose pairs are dealt across the CTAs in pieces of every kind:
+    pairs with more tiles than CTAs and a remainder (480 and 213 tiles), one-tile
+    pairs that each go to a single CTA, an empty pair, and a pair of 40 tiles, so the
+    CTA offsets of the pieces rotate through the grid."""
+    sizes = [(3000, 5000)] + [(100 + k, 90 + 3 * k) for k in range(20)] + [(0, 50), (2500, 300), (9000, 700)]
+    pairs_np = [S.make_pair(7, 66, k, max(na, 1), nb, 0.2, 0.05) for k, (na, nb) in enumerate(sizes)]
+    a_list = [p.a[:na] for p, (na, _) in zip(pairs_np, sizes)]
+    b_list = [p.b for p in pairs_np]
+    dev = [(_dev(a), _dev(b)) for a, b in zip(a_list, b_list)]
+    outs = serac.match_batch(dev, top2=True)
+    torch.cuda.synchronize()
+    for k in range(len(sizes)):
+        a, b = a_list[k], b_list[k]
+        ref = oracle_mod.match(a, b)
+        np.testing.assert_array_equal(outs[k].row_top2.cpu().numpy()[:a.shape[0]], ref.row_top2)
+        np.testing.assert_array_equal(outs[k].col_top2.cpu().numpy()[:b.shape[0]], ref.col_top2)
+        np.testing.assert_array_equal(outs[k].result().numpy(), ref.matches)
+
+
 @pytest.mark.parametrize("variant", ["default", "no_col_ratio", "no_mutual", "loose"])
 def test_ties_and_params(serac, oracle_mod, variant):
     rng = np.random.default_rng(11)
