@@ -353,8 +353,10 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     Segment g;
     while (next_segment(P, cur, g)) {
       const FusedPair& fp = P.pairs[g.p];
-      unsigned long long K1 = 0ull, K2 = 0ull;  // the row's top-2 over the segment
-      uint32_t thr = 0;                          // tile keys below this cannot enter
+      // the row's top-2 over the segment as tile keys (s << 8 | 255 - column in the
+      // tile) with the column tile each came from; 0 = empty
+      uint32_t R1 = 0u, R2 = 0u;
+      int C1 = 0, C2 = 0;
       for (int ct = g.ct0; ct < g.ct1; ++ct, ++tcount) {
         const uint32_t acc = tcount & 1u, aph = (tcount >> 1) & 1u;
         // on a timeout keep going (results are flagged invalid): every epilogue warp
@@ -362,6 +364,13 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
         if (!warp_wait(&t_full[acc], aph, abort_flag, P.err, ERR_TIMEOUT_EPILOGUE)) ok = false;
         tc_fence_after();
         const uint32_t par = tcount & 1u;
+        // the global second of the column this lane merges at the end of the tile,
+        // read from L2 now (it only grows, so any earlier value is a lower bound):
+        // a tile best below it changes neither slot and needs no atomics
+        const int mcol = ct * BN + qt * 64 + q * 16 + lane;
+        unsigned long long csec = ~0ull;
+        if (!DUMP && lane < 16 && mcol < fp.n_b)
+          csec = __ldcg(P.colkeys + 2 * static_cast<int64_t>(fp.col_base + mcol) + 1);
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + qt * 64;
         float t1 = 0.f, t2 = 0.f;  // the row's top-2 over this tile (8-bit column index)
 #pragma unroll
@@ -418,13 +427,21 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&t_empty[acc]);
         if constexpr (!DUMP) {
-          // row: fold the tile's top-2 into the segment's (rarely taken after a few tiles)
+          // row: fold the tile's top-2 into the segment's.  Tiles come in column
+          // order, so a tile key displaces a held one only with a strictly larger
+          // score (k > (R | 255)); on equal scores the earlier, lower column stays.
           const uint32_t k1t = __float_as_uint(t1), k2t = __float_as_uint(t2);
-          if (k1t >= thr) {
-            const uint32_t base = static_cast<uint32_t>(ct * BN);
-            ins2_64(K1, K2, key64(k1t, base));
-            ins2_64(K1, K2, key64(k2t, base));
-            thr = static_cast<uint32_t>(K2 >> 32) << 8;
+          if (k1t > (R2 | 255u)) {
+            if (k1t > (R1 | 255u)) {
+              const bool t2_wins = k2t > (R1 | 255u);
+              R2 = t2_wins ? k2t : R1;
+              C2 = t2_wins ? ct : C1;
+              R1 = k1t;
+              C1 = ct;
+            } else {
+              R2 = k1t;
+              C2 = ct;
+            }
           }
           // columns: merge the four row quadrants once all four have written
           named_bar_sync(1 + qt, 128);  // the four quadrant warps of this quarter
@@ -447,7 +464,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
               const uint32_t rbase = static_cast<uint32_t>(g.rt * BM);
               const unsigned long long x1 = key64(__float_as_uint(m1), rbase);
               const unsigned long long x2 = key64(__float_as_uint(m2), rbase);
-              if (x1) {
+              if (x1 > csec) {
                 unsigned long long* ck = P.colkeys + 2 * static_cast<int64_t>(fp.col_base + j);
                 pend_old = atomicMax(ck, x1);
                 pend_x1 = x1;
@@ -465,6 +482,8 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
           rpend_ptr = nullptr;
         }
         const int i = g.rt * BM + static_cast<int>(rl);
+        const unsigned long long K1 = key64(R1, static_cast<uint32_t>(C1 * BN));
+        const unsigned long long K2 = key64(R2, static_cast<uint32_t>(C2 * BN));
         if (ok && i < fp.n_a && K1) {
           unsigned long long* rk = P.rowkeys + 2 * static_cast<int64_t>(fp.row_base + i);
           rpend_old = atomicMax(rk, K1);
