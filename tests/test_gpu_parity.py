@@ -118,8 +118,9 @@ def test_largest_size(serac, oracle_mod):
 
 @pytest.mark.parametrize("na,nb", [(128, 65536), (100, 40000), (65536, 200), (40000, 130)])
 def test_extreme_aspect(serac, oracle_mod, na, nb):
-    """One row tile against hundreds of column tiles (every tile its own work item, rows
-    merged across many CTAs), and the transpose (hundreds of row tiles, one column tile)."""
+    """One row tile against hundreds of column tiles (the row tile split over many CTAs,
+    rows merged across them), and the reverse (hundreds of row tiles, one column tile:
+    every column merged from hundreds of CTAs)."""
     p = S.make_pair(4, 63, na + nb, na, nb, 0.3, 0.05)
     _assert_pair(serac, oracle_mod, p.a, p.b)
 

@@ -6,10 +6,10 @@
 // per-block partials for the cross check.  This kernel keeps that dataflow but forms
 // the dot products on the sm_103a tensor cores instead of DP4A:
 //
-//   * a persistent CTA per SM walks a contiguous range of work items; consecutive
-//     items on the same row tile form a segment: one 128-row tile of A resident in
-//     shared memory against a run of 256-row tiles of B streamed by TMA (128-byte
-//     swizzle, two stages);
+//   * a persistent CTA per SM takes one contiguous piece (a row-major run of
+//     128 x 256 tiles) of every pair of the launch; the tiles of a piece on one row
+//     tile form a segment: one 128-row tile of A resident in shared memory against a
+//     run of 256-row tiles of B streamed by TMA (128-byte swizzle, two stages);
 //   * one thread issues tcgen05.mma kind::f16 (bf16 x bf16 -> f32, M=128, N=256,
 //     K=16 x 8) into one of two TMEM accumulators (2 x 256 columns), so the epilogue
 //     of tile t overlaps the MMAs of tile t+1.  u8 values are exact in bf16 and every
@@ -28,10 +28,10 @@
 //         3-input float max can merge them;
 //       - reduce each 16-key sub-chunk with a tree (for instruction-level parallelism)
 //         and keep the row top-2 in registers across the segment,
-//       - transpose column keys through shared memory in 16-column half-blocks,
-//         take the top-2 of every column over the warp's 32 rows (two lanes per
-//         column, one shuffle), merge the four row quadrants,
-//         and fold the tile's column top-2 into the column's global top-2 with 64-bit
+//       - take the top-2 of every column over the warp's 32 rows with two warp-wide
+//         max reductions per column (the second as the max of key - best, which
+//         wraps the best to 0), merge the four row quadrants in shared memory, and
+//         fold the tile's column top-2 into the column's global top-2 with 64-bit
 //         atomicMax ("Wider tiles": the column partials, here merged in place).
 //
 // Global top-2 by atomics: old = max(best, x1); second = max(second, min(old, x1));
@@ -59,13 +59,10 @@ constexpr int B_BYTES = BN * KDIM * 2;   // 64 KB
 constexpr int B_HALF = BN * 64 * 2;      // 32 KB
 constexpr int BOX_BYTES = 128 * 64 * 2;  // 16 KB: one TMA box (64 x 128)
 constexpr int NUM_EPI_WARPS = 16;
-constexpr int T_STRIDE = 36;             // transpose half-block: 16 columns x 36 words (padded)
-constexpr int T_WARP_WORDS = 16 * T_STRIDE;
 
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + A_BYTES;
-constexpr int OFF_T = OFF_B + 2 * B_BYTES;
-constexpr int OFF_M = OFF_T + NUM_EPI_WARPS * T_WARP_WORDS * 4;
+constexpr int OFF_M = OFF_B + 2 * B_BYTES;
 constexpr int M_BYTES = 2 * 4 * BN * 8;  // [parity][quadrant][column] (k1, k2)
 constexpr int OFF_BAR = OFF_M + M_BYTES;
 constexpr int BAR_BYTES = 256;
@@ -333,12 +330,6 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     // (per-thread index) take 256 from a kernel parameter so the compiler keeps them
     // one multiply-add on the FMA pipe, off the busier ALU
     const uint32_t key_mult = P.key_mult;
-    const int rd_col = lane & 15, rd_half = lane >> 4;          // transposed read: column, row half
-    // transpose block: written row-wise (lane = row), read column-wise
-    uint32_t* tb_w = reinterpret_cast<uint32_t*>(smem + OFF_T) + e * T_WARP_WORDS + lane;
-    const uint4* tb_r =
-        reinterpret_cast<const uint4*>(reinterpret_cast<uint32_t*>(smem + OFF_T) + e * T_WARP_WORDS +
-                                       rd_col * T_STRIDE + rd_half * 16);
     uint2* sm = reinterpret_cast<uint2*>(smem + OFF_M);
     uint32_t tcount = 0;
     bool ok = true;
@@ -398,25 +389,19 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
               for (int k = 0; k < 16; ++k) rk[k] = __uint_as_float((v[k] << 8) + (15u - k));
               tree_top2(rk, a1, a2);
             }
-            // columns: the 16 x 32 block goes through shared memory and back transposed
+            // columns: the warp's best key per column is a warp-wide max; the second is
+            // the max of (key - best), which wraps the best lane to 0 and keeps the
+            // order of the others.  Lane 0 stores the 16 columns' (best, second - best)
+            // (mod 2^32); the quadrant merge adds the best back.
+            uint4* sm4 = reinterpret_cast<uint4*>(sm + (par * 4 + q) * BN + qt * 64 + c * 16);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) tb_w[k * T_STRIDE] = mad_lo(v[k], key_mult, col_low);
-            __syncwarp();
-            float xs[16];
-#pragma unroll
-            for (int r4 = 0; r4 < 4; ++r4) {
-              const uint4 x = tb_r[r4];
-              xs[4 * r4 + 0] = __uint_as_float(x.x);
-              xs[4 * r4 + 1] = __uint_as_float(x.y);
-              xs[4 * r4 + 2] = __uint_as_float(x.z);
-              xs[4 * r4 + 3] = __uint_as_float(x.w);
+            for (int k = 0; k < 16; k += 2) {
+              const uint32_t x0 = mad_lo(v[k], key_mult, col_low), x1 = mad_lo(v[k + 1], key_mult, col_low);
+              const uint32_t m0 = __reduce_max_sync(0xffffffffu, x0), m1 = __reduce_max_sync(0xffffffffu, x1);
+              const uint32_t s0 = __reduce_max_sync(0xffffffffu, x0 - m0);
+              const uint32_t s1 = __reduce_max_sync(0xffffffffu, x1 - m1);
+              if (lane == 0) sm4[k >> 1] = make_uint4(m0, s0, m1, s1);
             }
-            __syncwarp();
-            float c1, c2;
-            tree_top2(xs, c1, c2);
-            merge2(c1, c2, __shfl_xor_sync(0xffffffffu, c1, 16), __shfl_xor_sync(0xffffffffu, c2, 16));
-            if (lane < 16)
-              sm[(par * 4 + q) * BN + qt * 64 + c * 16 + rd_col] = make_uint2(__float_as_uint(c1), __float_as_uint(c2));
             // sub-chunk index (15 - k) -> tile-local 255 - (64 qt + 16 c + k)
             const uint32_t chb = static_cast<uint32_t>(15 - 4 * qt - c) << 4;
             merge2(t1, t2, __uint_as_float(__float_as_uint(a1) | chb), __uint_as_float(__float_as_uint(a2) | chb));
@@ -453,11 +438,11 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
           if (lane < 16) {
             const int col = qt * 64 + q * 16 + lane;
             uint2 x = sm[(par * 4 + 0) * BN + col];
-            float m1 = __uint_as_float(x.x), m2 = __uint_as_float(x.y);
+            float m1 = __uint_as_float(x.x), m2 = __uint_as_float(x.y + x.x);
 #pragma unroll
             for (int qq = 1; qq < 4; ++qq) {
               x = sm[(par * 4 + qq) * BN + col];
-              merge2(m1, m2, __uint_as_float(x.x), __uint_as_float(x.y));
+              merge2(m1, m2, __uint_as_float(x.x), __uint_as_float(x.y + x.x));
             }
             const int j = ct * BN + col;
             if (j < fp.n_b) {
