@@ -325,10 +325,9 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     const int qt = e >> 2;        // which 64-column quarter of the tile
     const uint32_t rl = static_cast<uint32_t>(q * 32 + lane);  // row within the tile
     const uint32_t col_low = 255u - rl;                         // column keys carry the row
-    // keys are u * 256 + index bits (the multiply shifts the exponent bits out).  Row
-    // keys (immediate index) are one shift-and-add on the integer ALU; column keys
-    // (per-thread index) take 256 from a kernel parameter so the compiler keeps them
-    // one multiply-add on the FMA pipe, off the busier ALU
+    // keys are u * 256 + index bits (the multiply shifts the exponent bits out).  Both
+    // take 256 from a kernel parameter so that the compiler keeps them one integer
+    // multiply-add each on the FMA pipe: the min/max trees keep the ALU pipe busy
     const uint32_t key_mult = P.key_mult;
     uint2* sm = reinterpret_cast<uint2*>(smem + OFF_M);
     uint32_t tcount = 0;
@@ -386,7 +385,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
             {
               float rk[16];
 #pragma unroll
-              for (int k = 0; k < 16; ++k) rk[k] = __uint_as_float((v[k] << 8) + (15u - k));
+              for (int k = 0; k < 16; ++k) rk[k] = __uint_as_float(mad_lo(v[k], key_mult, 15u - k));
               tree_top2(rk, a1, a2);
             }
             // columns: the warp's best key per column is a warp-wide max; the second is
