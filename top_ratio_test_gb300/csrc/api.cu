@@ -31,6 +31,7 @@ size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 
 struct Chunk {
   int p0 = 0, p1 = 0;          // pairs [p0, p1)
+  int img0 = 0, img1 = 0;      // images first used by this chunk: [img0, img1)
   int64_t tiles = 0;           // 128 x 256 tiles of all its pairs
   int64_t rows = 0, cols = 0;  // sum of n_a, n_b
   int64_t blocks = 0;          // match-kernel blocks
@@ -93,7 +94,11 @@ void build_plan(const serac_pair* pairs, int32_t n_pairs, Plan& pl) {
       ++p;
     }
     ch.p1 = p;
+    // images are numbered in order of first use, so each chunk's new ones are a range
+    ch.img0 = pl.chunks.empty() ? 0 : pl.chunks.back().img1;
+    ch.img1 = ch.img0;
     for (int k = ch.p0; k < ch.p1; ++k) {
+      ch.img1 = std::max({ch.img1, pl.a_img[k] + 1, pl.b_img[k] + 1});
       ch.tiles += pair_tiles(pairs[k]);
       ch.rows += pairs[k].n_a;
       ch.cols += pairs[k].n_b;
@@ -214,6 +219,33 @@ int encode_staged_map(CUtensorMap* map, void* staged, int64_t rows) {
 }
 
 cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
+
+// Per host thread and device: a side stream on which match_batch stages the images of
+// its later launch chunks while the earlier chunks compute, and the events that order
+// it (one for the call's start, one per staged chunk).
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t start = nullptr;
+  std::vector<cudaEvent_t> staged;
+};
+constexpr int MAX_DEVICES = 64;
+thread_local SideStream t_side[MAX_DEVICES];
+
+int side_stream(size_t n_events, SideStream** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return SERAC_ECUDA;
+  SideStream& s = t_side[dev];
+  if (!s.stream && (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess ||
+                    cudaEventCreateWithFlags(&s.start, cudaEventDisableTiming) != cudaSuccess))
+    return SERAC_ECUDA;
+  while (s.staged.size() < n_events) {
+    cudaEvent_t e;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return SERAC_ECUDA;
+    s.staged.push_back(e);
+  }
+  *out = &s;
+  return SERAC_OK;
+}
 bool g_inject_no_copies = false;  // consumed by the next call's first fused launch
 int g_last_launches = 0;
 int g_last_cuda_error = 0;
@@ -277,28 +309,51 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
     if (st != SERAC_OK) return st;
   }
 
-  // staging (512 images per launch); the first launch also clears the error word and
-  // the key arrays, which every match launch leaves cleared behind it
-  for (size_t i0 = 0; i0 == 0 || i0 < pl.images.size(); i0 += 512) {
+  // staging, one launch per chunk for the images it uses first (at most 256).  The
+  // first launch also clears the error word and the key arrays, which every match
+  // launch leaves cleared behind it.  With several chunks, the later chunks' images
+  // are staged on a side stream while the earlier chunks compute (their host reads
+  // overlap the kernels); each chunk's fused launch waits for its own staging.
+  const bool overlap = pl.chunks.size() > 1 && !dump;
+  SideStream* side = nullptr;
+  std::vector<char> on_side(pl.chunks.size(), 0);  // chunk staged on the side stream
+  if (overlap) {
+    st = side_stream(pl.chunks.size(), &side);
+    if (st != SERAC_OK) return st;
+  }
+  for (size_t ci = 0; ci < pl.chunks.size(); ++ci) {
+    const Chunk& ch = pl.chunks[ci];
     StageParams sp;
     std::memset(&sp, 0, sizeof(sp));
     sp.staged = staged;
     sp.err = err;
-    if (i0 == 0) {
+    if (ci == 0) {
       sp.zero = reinterpret_cast<uint4*>(ws + pl.off_region[0]);
       sp.zero_n = static_cast<int64_t>((pl.total - pl.off_region[0]) / 16);
       sp.zero_blocks = static_cast<int32_t>(std::min<int64_t>(1024, (sp.zero_n + 255) / 256));
       if (sp.zero_blocks < 1) sp.zero_blocks = 1;
     }
     int64_t max_chunks = 0;
-    for (size_t i = i0; i < pl.images.size() && i < i0 + 512; ++i) {
+    for (int i = ch.img0; i < ch.img1; ++i) {
       if (pl.images[i].n == 0) continue;
       sp.images[sp.n_images++] = pl.images[i];
       max_chunks = std::max<int64_t>(max_chunks, round_up(pl.images[i].n, PAD_ROWS) * (KDIM / 16));
     }
-    if (sp.n_images == 0 && i0 > 0) continue;
-    SERAC_TRY_CUDA(static_cast<cudaError_t>(launch_stage(sp, max_chunks, stream)));
+    if (ci > 0 && sp.n_images == 0) continue;
+    void* s_stage = (ci == 0 || !overlap) ? stream : static_cast<void*>(side->stream);
+    SERAC_TRY_CUDA(static_cast<cudaError_t>(launch_stage(sp, max_chunks, s_stage, s_stage != stream)));
     ++g_last_launches;
+    if (ci == 0 && overlap) {
+      // the side stream starts once the first chunk is staged: it then has the host
+      // link to itself while the first chunk computes, and the work queued earlier on
+      // `stream` (a previous call with this workspace) is done
+      SERAC_TRY_CUDA(cudaEventRecord(side->start, static_cast<cudaStream_t>(stream)));
+      SERAC_TRY_CUDA(cudaStreamWaitEvent(side->stream, side->start, 0));
+    }
+    if (ci > 0 && overlap) {
+      SERAC_TRY_CUDA(cudaEventRecord(side->staged[ci], side->stream));
+      on_side[ci] = 1;
+    }
   }
 
   bool first_fused = true;
@@ -308,6 +363,8 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
     uint8_t* other = ws + pl.off_region[(ci + 1) & 1];
     unsigned long long* rowkeys = reinterpret_cast<unsigned long long*>(region + pl.r_rowkeys);
     unsigned long long* colkeys = reinterpret_cast<unsigned long long*>(region + pl.r_colkeys);
+    // this chunk's images (staged on the side stream) must be in place
+    if (on_side[ci]) SERAC_TRY_CUDA(cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), side->staged[ci], 0));
     // ---------------- fused GEMM + top-2, merged into the key arrays
     if (ch.tiles > 0) {
       FusedParams fp;

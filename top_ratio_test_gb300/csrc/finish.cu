@@ -219,13 +219,18 @@ __global__ void __launch_bounds__(MATCH_THREADS) match_kernel(const __grid_const
 
 }  // namespace
 
-int launch_stage(const StageParams& p, int64_t max_chunks, void* stream) {
-  int64_t blocks = (max_chunks + 255) / 256;
-  if (blocks > 1024) blocks = 1024;
+int launch_stage(const StageParams& p, int64_t max_chunks, void* stream, bool beside_fused) {
+  // Beside a running fused kernel (one CTA of 18 warps x 96 registers per SM) an SM
+  // sub-partition holding five of its warps has 1,024 registers left: one warp of 32
+  // registers.  Blocks of four warps (one per sub-partition) then fit beside it; blocks
+  // of eight would wait for the fused kernel to end.
+  const int threads = beside_fused ? 128 : 256;
+  int64_t blocks = (max_chunks + threads - 1) / threads;
+  if (blocks > 2048) blocks = 2048;
   if (blocks < p.zero_blocks) blocks = p.zero_blocks;
   if (blocks < 1) blocks = 1;
-  stage_kernel<<<dim3(static_cast<unsigned>(blocks), p.n_images + 1), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      p);
+  stage_kernel<<<dim3(static_cast<unsigned>(blocks), p.n_images + 1), threads, 0,
+                 static_cast<cudaStream_t>(stream)>>>(p);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -110,7 +110,7 @@ struct FinishParams {
 };
 
 // launchers (defined in fused.cu / finish.cu); return a cudaError_t value
-int launch_stage(const StageParams& p, int64_t max_chunks, void* stream);
+int launch_stage(const StageParams& p, int64_t max_chunks, void* stream, bool beside_fused);
 int launch_fused(const FusedParams& p, const void* tmap, bool dump, void* stream);
 int launch_match(const FinishParams& p, void* stream);
 int fused_smem_bytes();
