@@ -120,7 +120,12 @@ size_t match_batch_workspace_size(const serac_pair* pairs, int32_t n_pairs);
 
 /* Match every pair of `pairs` (host array) into outs[k] (host array of device
  * outputs).  Equivalent to match_pair on each pair in turn, scheduled as a few
- * persistent launches over all pairs' tiles.  Same workspace rules as match_pair. */
+ * persistent launches over all pairs' tiles.  Same workspace rules as match_pair.
+ * The pairs run in launch chunks of at most 128; each chunk's images are staged
+ * before its launch, the later chunks' on an internal per-thread stream while the
+ * earlier chunks compute (the call still only orders work on `cuda_stream`: the
+ * internal stream starts after the work already queued there, and the launches that
+ * need its staging wait for it). */
 int match_batch(const serac_pair* pairs, int32_t n_pairs, const serac_params* params,
                 const serac_out* outs, void* workspace, size_t workspace_bytes,
                 void* cuda_stream);

@@ -284,6 +284,26 @@ def test_batch_host_buffers_and_reuse(serac, oracle_mod):
         torch.cuda.synchronize()
 
 
+def test_batch_host_images_over_chunks(serac, oracle_mod):
+    """188 pairs of 16 shared pinned host images: two launch chunks, the second
+    chunk's new images staged on the side stream while the first computes, and its
+    pairs also reusing images the first chunk staged."""
+    imgs_np = [S.make_pair(8, 71, k, 300 + 97 * k, 10, 0.0, 0.05).a for k in range(16)]
+    for k in range(15):  # plant rows of image k into image k + 1
+        imgs_np[k + 1][: 150] = imgs_np[k][50:200]
+    imgs = [torch.from_numpy(x).pin_memory() for x in imgs_np]
+    idx = [(i, j) for i in range(12) for j in range(12) if i != j][:128]   # chunk 0: images 0..11
+    idx += [(i, j) for i in range(12, 16) for j in range(16) if i != j][:72]  # chunk 1 adds 12..15
+    pairs = [(imgs[i], imgs[j]) for i, j in idx]
+    outs = serac.match_batch(pairs, top2=True)
+    torch.cuda.synchronize()
+    for k, (i, j) in enumerate(idx):
+        ref = oracle_mod.match(imgs_np[i], imgs_np[j])
+        np.testing.assert_array_equal(outs[k].row_top2.cpu().numpy(), ref.row_top2)
+        np.testing.assert_array_equal(outs[k].col_top2.cpu().numpy(), ref.col_top2)
+        np.testing.assert_array_equal(outs[k].result().numpy(), ref.matches)
+
+
 def test_batch_ragged_256(serac, oracle_mod):
     """256 ragged pairs (1,000..16,384 features): 12 pairs checked in full, every
     pair checked on 48 sampled rows (top-2 and decision) and 48 sampled columns."""
