@@ -227,6 +227,11 @@ struct SideStream {
   cudaStream_t stream = nullptr;
   cudaEvent_t start = nullptr;
   std::vector<cudaEvent_t> staged;
+  ~SideStream() {  // at thread exit; errors (a runtime already shut down) are ignored
+    for (cudaEvent_t e : staged) cudaEventDestroy(e);
+    if (start) cudaEventDestroy(start);
+    if (stream) cudaStreamDestroy(stream);
+  }
 };
 constexpr int MAX_DEVICES = 64;
 thread_local SideStream t_side[MAX_DEVICES];
