@@ -304,6 +304,54 @@ def test_batch_host_images_over_chunks(serac, oracle_mod):
         np.testing.assert_array_equal(outs[k].result().numpy(), ref.matches)
 
 
+def test_batch_concurrent_host_threads(serac, oracle_mod):
+    """Two host threads run multi-chunk batches at the same time, each on its own
+    stream and workspace (each thread stages its later chunks on its own side stream);
+    a third batch runs on the legacy default stream.  Every output equals the oracle."""
+    import threading
+    imgs_np = [S.make_pair(9, 72, k, 200 + 61 * k, 10, 0.0, 0.05).a for k in range(13)]
+    for k in range(12):
+        imgs_np[k + 1][: 100] = imgs_np[k][20:120]
+    refs = {}
+    # 156 pairs in two chunks; image 12 is first used by the second chunk
+    order = sorted(((i, j) for i in range(13) for j in range(13) if i != j), key=lambda t: (max(t), t))
+
+    def batch(kind):
+        imgs = [torch.from_numpy(x).pin_memory() if kind == "host" else _dev(x) for x in imgs_np]
+        return order, [(imgs[i], imgs[j]) for i, j in order]
+
+    results, errors = {}, []
+
+    def worker(name, kind):
+        try:
+            idx, pairs = batch(kind)
+            st = torch.cuda.Stream()
+            ws = serac.workspace(serac.batch_workspace_size(pairs), torch.device("cuda", 0))
+            outs = None
+            for _ in range(3):
+                outs = serac.match_batch(pairs, workspace_t=ws, stream=st, outs=outs)
+            st.synchronize()
+            results[name] = (idx, outs)
+        except Exception as exc:  # reported by the main thread
+            errors.append(exc)
+
+    threads = [threading.Thread(target=worker, args=(n, k)) for n, k in (("t0", "host"), ("t1", "device"))]
+    for t in threads:
+        t.start()
+    idx, pairs = batch("device")
+    legacy = serac.match_batch(pairs, stream=torch.cuda.default_stream())
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    results["legacy"] = (idx, legacy)
+    for name, (idx, outs) in results.items():
+        for k, (i, j) in enumerate(idx):
+            if (i, j) not in refs:
+                refs[(i, j)] = oracle_mod.match(imgs_np[i], imgs_np[j]).matches
+            np.testing.assert_array_equal(outs[k].result().numpy(), refs[(i, j)], err_msg=f"{name} pair {k}")
+
+
 def test_batch_ragged_256(serac, oracle_mod):
     """256 ragged pairs (1,000..16,384 features): 12 pairs checked in full, every
     pair checked on 48 sampled rows (top-2 and decision) and 48 sampled columns."""
