@@ -1,5 +1,5 @@
 // C ABI of libserac_gb300: argument checks, image staging plan, workspace layout,
-// the work-item schedule of the persistent fused kernel, and the launch sequence.
+// the work schedule of the persistent fused kernel, and the launch sequence.
 //
 // Schedule.  Pairs are processed in launch chunks of at most MAX_PAIRS pairs (the
 // per-pair tables travel as kernel parameters, so a call needs no host-to-device
