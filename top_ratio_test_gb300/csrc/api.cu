@@ -452,6 +452,10 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
     }
     fn.n_pairs = np;
     fn.total_blocks = static_cast<int32_t>(blocks);
+    // a grid of at most one block per SM has every block resident once the fused
+    // kernel is done, so blocks may take their order from the block index (no ticket
+    // round trip); larger grids keep the tickets (a block only waits on started ones)
+    fn.index_order = blocks <= sms ? 1 : 0;
     if (np > 0) {
       SERAC_TRY_CUDA(static_cast<cudaError_t>(launch_match(fn, stream)));
       ++g_last_launches;

@@ -102,6 +102,8 @@ struct FinishParams {
   const unsigned long long* rowkeys;
   const unsigned long long* colkeys;
   int32_t* tickets;               // [pair]: next block index of the pair (zeroed)
+  int32_t index_order;            // 1: block order = block index (the whole grid fits the GPU)
+  int32_t pad_;
   unsigned long long* status;     // [block]: look-back word (zeroed)
   uint4* zero;                    // the other chunk's key region, cleared here
   int64_t zero_n;                 // 16-byte words
