@@ -383,6 +383,11 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
       fp.dump = dump;
       fp.dump_ld = (dump && n_pairs > 0) ? pairs[0].n_b : 0;
       fp.key_mult = 256u;
+      // the last chunk's match grid, if it has at most one block per SM, may start
+      // beside the fused CTAs (its blocks fit there) and wait for them
+      int64_t mblocks = 0;
+      for (int k = ch.p0; k < ch.p1; ++k) mblocks += match_blocks(pairs[k].n_a);
+      fp.early_dependents = (!dump && ci + 1 == pl.chunks.size() && mblocks <= sms) ? 1 : 0;
       fp.no_copies = (first_fused && g_inject_no_copies) ? 1 : 0;
       if (first_fused) g_inject_no_copies = false;
       int np = 0;

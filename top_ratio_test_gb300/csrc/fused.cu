@@ -233,6 +233,8 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     fence_proxy_async_smem();
   }
   __syncthreads();
+  // a small match launch may be placed beside the CTAs now; it waits for this grid
+  if (P.early_dependents) grid_dep_launch();
   // everything above overlaps the staging kernel (programmatic dependent launch);
   // the staged operands, the cleared keys and the error word are read after this
   grid_dep_wait();

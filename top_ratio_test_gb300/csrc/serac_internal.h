@@ -58,6 +58,7 @@ struct FusedParams {
   int32_t* dump;                     // score dump (dump mode only)
   uint32_t key_mult;                 // 256, read as a kernel parameter (see the epilogue)
   int32_t no_copies;                 // test hook: the producer issues no copies (bounded waits run out)
+  int32_t early_dependents;          // let the match launch start beside this kernel's CTAs
   FusedPair pairs[MAX_PAIRS];
 };
 
@@ -91,7 +92,7 @@ struct FinishPair {
   int32_t pad_;
 };
 
-constexpr int MATCH_THREADS = 256;
+constexpr int MATCH_THREADS = 128;
 constexpr int MATCH_ROWS_PER_THREAD = 2;
 constexpr int MATCH_ROWS_PER_BLOCK = MATCH_THREADS * MATCH_ROWS_PER_THREAD;
 
