@@ -63,7 +63,7 @@ constexpr int NUM_EPI_WARPS = 16;
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + A_BYTES;
 constexpr int OFF_M = OFF_B + 2 * B_BYTES;
-constexpr int M_BYTES = 2 * 4 * BN * 8;  // [parity][quadrant][column] (k1, k2)
+constexpr int M_BYTES = 2 * 4 * BN * 8;  // [parity][quadrant][column] (k1, k2 - k1 mod 2^32)
 constexpr int OFF_BAR = OFF_M + M_BYTES;
 constexpr int BAR_BYTES = 256;
 // bias operands of the first MMA of every tile (no swizzle, one 8-row group read by
