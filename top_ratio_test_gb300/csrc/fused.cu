@@ -359,9 +359,12 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
         // the global second of the column this lane merges at the end of the tile,
         // read from L2 now (it only grows, so any earlier value is a lower bound):
         // a tile best below it changes neither slot and needs no atomics
-        const int mcol = ct * BN + qt * 64 + q * 16 + lane;
+        // this tile's quadrant merge is done by two of the quarter's four warps (which two
+        // alternates by tile), 32 columns each
+        const bool merger = (q & 1) == static_cast<int>(tcount & 1u);
+        const int mcol = ct * BN + qt * 64 + (q >> 1) * 32 + lane;
         unsigned long long csec = ~0ull;
-        if (!DUMP && lane < 16 && mcol < fp.n_b)
+        if (!DUMP && merger && mcol < fp.n_b)
           csec = __ldcg(P.colkeys + 2 * static_cast<int64_t>(fp.col_base + mcol) + 1);
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + qt * 64;
         float t1 = 0.f, t2 = 0.f;  // the row's top-2 over this tile (8-bit column index)
@@ -436,8 +439,8 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
             if (lo) atomicMax(pend_ptr, lo);
             pend_ptr = nullptr;
           }
-          if (lane < 16) {
-            const int col = qt * 64 + q * 16 + lane;
+          if (merger) {
+            const int col = qt * 64 + (q >> 1) * 32 + lane;
             uint2 x = sm[(par * 4 + 0) * BN + col];
             float m1 = __uint_as_float(x.x), m2 = __uint_as_float(x.y + x.x);
 #pragma unroll
