@@ -167,14 +167,6 @@ __device__ __forceinline__ unsigned long long key64(uint32_t k, uint32_t base) {
   return (static_cast<unsigned long long>(s) << 32) | (0xFFFFFFFFu - idx);
 }
 
-// Bounded wait by lane 0, result broadcast to the warp.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
-                                          int code) {
-  int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, err, code, WAIT_LIMIT_NS) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
 template <bool DUMP>
 __global__ void __launch_bounds__(FUSED_THREADS, 1)
     fused_top2_kernel(const __grid_constant__ FusedParams P, const __grid_constant__ CUtensorMap tmap) {
@@ -353,7 +345,10 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
         const uint32_t acc = tcount & 1u, aph = (tcount >> 1) & 1u;
         // on a timeout keep going (results are flagged invalid): every epilogue warp
         // must pass the same named-barrier sequence
-        if (!warp_wait(&t_full[acc], aph, abort_flag, P.err, ERR_TIMEOUT_EPILOGUE)) ok = false;
+        {  // every lane tests the barrier (no broadcast), one vote for the outcome
+          const bool w = mbar_wait(&t_full[acc], aph, abort_flag, P.err, ERR_TIMEOUT_EPILOGUE, WAIT_LIMIT_NS);
+          if (!__all_sync(0xffffffffu, w)) ok = false;
+        }
         tc_fence_after();
         const uint32_t par = tcount & 1u;
         // the global second of the column this lane merges at the end of the tile,
