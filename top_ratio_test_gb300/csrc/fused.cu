@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
       mbar_init(&b_full[i], 1);
       mbar_init(&b_empty[i], 1);
       mbar_init(&t_full[i], 1);
-      mbar_init(&t_empty[i], NUM_EPI_WARPS);
+      mbar_init(&t_empty[i], NUM_EPI_WARPS * 32);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -406,10 +406,9 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
             merge2(t1, t2, __uint_as_float(__float_as_uint(a1) | chb), __uint_as_float(__float_as_uint(a2) | chb));
           }
         }
-        // hand the buffer back to the MMA
+        // hand the buffer back to the MMA: every thread once its own loads are done
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&t_empty[acc]);
+        mbar_arrive(&t_empty[acc]);
         if constexpr (!DUMP) {
           // row: fold the tile's top-2 into the segment's.  Tiles come in column
           // order, so a tile key displaces a held one only with a strictly larger
