@@ -53,7 +53,7 @@ WORKLOAD_2000 = "single pair 2000x2000 SIFT-shaped u8 descriptors, 30% planted a
 # DRAM bytes (read + write) of one fused_top2_kernel launch on the 8192 x 8192 pair, from
 # the ncu capture summarised in profiles/fused_top2_pair_8192x8192_full.md; None whenever
 # the kernel has changed since that capture
-FUSED_TRAFFIC_8192 = None
+FUSED_TRAFFIC_8192 = 4492288
 
 
 def _peaks():
