@@ -21,7 +21,9 @@ namespace serac {
 
 namespace {
 
-__global__ void __launch_bounds__(256) stage_kernel(const __grid_constant__ StageParams P) {
+// At most 32 registers per thread (256 threads x 8 blocks): four-warp blocks then fit
+// beside a fused CTA (see launch_stage).
+__global__ void __launch_bounds__(256, 8) stage_kernel(const __grid_constant__ StageParams P) {
   grid_dep_launch();  // the fused kernel may start its prologue alongside the last blocks
   if (blockIdx.y == static_cast<unsigned>(P.n_images)) {
     // clear the key arrays and the error word
@@ -84,7 +86,9 @@ __device__ __forceinline__ uint64_t now_ns() {
   return t;
 }
 
-__global__ void __launch_bounds__(MATCH_THREADS) match_kernel(const __grid_constant__ FinishParams P) {
+// At most 32 registers per thread, so that the four-warp blocks fit beside a fused CTA.
+__global__ void __launch_bounds__(MATCH_THREADS, 65536 / (MATCH_THREADS * 32)) match_kernel(
+    const __grid_constant__ FinishParams P) {
   // launched early (programmatic dependent launch): wait for the fused kernel's keys
   grid_dep_wait();
   // this block's pair
