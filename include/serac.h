@@ -147,12 +147,12 @@ int serac_set_profile_events(void* ev_begin, void* ev_end);
  * else SERAC_EUNSUPPORTED (or SERAC_ECUDA if no device can be queried). */
 int serac_device_check(void);
 
-/* Number of kernel launches the last match_pair / match_batch call enqueued
- * (host-side count, for benchmarking). */
+/* Number of kernel launches the calling thread's last match_pair / match_batch call
+ * enqueued (host-side count, for benchmarking). */
 int serac_last_launch_count(void);
 
-/* The cudaError_t value behind the last SERAC_ECUDA this library returned (0 if
- * none), for diagnostics. */
+/* The cudaError_t value behind the last SERAC_ECUDA this library returned to the
+ * calling thread (0 if none), for diagnostics. */
 int serac_last_cuda_error(void);
 
 /* Failure-detection test hook.  With enable != 0, the next match_pair / match_batch

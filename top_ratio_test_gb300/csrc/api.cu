@@ -252,8 +252,8 @@ int side_stream(size_t n_events, SideStream** out) {
   return SERAC_OK;
 }
 bool g_inject_no_copies = false;  // consumed by the next call's first fused launch
-int g_last_launches = 0;
-int g_last_cuda_error = 0;
+thread_local int g_last_launches = 0;    // per calling thread
+thread_local int g_last_cuda_error = 0;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
