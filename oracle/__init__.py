@@ -43,7 +43,8 @@ def build_library(force: bool = False) -> str:
 class _Params(ctypes.Structure):
     _fields_ = [("ratio_num_sq", ctypes.c_int64), ("ratio_den_sq", ctypes.c_int64),
                 ("norm_sq", ctypes.c_int64), ("min_score", ctypes.c_int64),
-                ("mutual", ctypes.c_int32), ("col_ratio", ctypes.c_int32)]
+                ("mutual", ctypes.c_int32), ("col_ratio", ctypes.c_int32),
+                ("max_features", ctypes.c_int32)]
 
 
 @dataclass(frozen=True)
@@ -55,14 +56,15 @@ class Params:
     min_score: int = 200499
     mutual: int = 1
     col_ratio: int = 1
+    max_features: int = 0  # K > 0: each image takes part with its first K descriptors
 
     def _c(self) -> _Params:
         return _Params(self.ratio_num_sq, self.ratio_den_sq, self.norm_sq,
-                       self.min_score, self.mutual, self.col_ratio)
+                       self.min_score, self.mutual, self.col_ratio, self.max_features)
 
 
 def default_params(max_ratio: float = 0.8, max_angle: float = 0.7,
-                   mutual: int = 1, col_ratio: int = 1) -> Params:
+                   mutual: int = 1, col_ratio: int = 1, max_features: int = 0) -> Params:
     """0.8 / 0.7 rad -> r^2 = 16/25 and min_score = ceil(cos(0.7) * 512^2) = 200499.
 
     max_ratio is read to 4 decimals (r = R / 10^4) and r^2 = R^2 / 10^8 is reduced.
@@ -72,7 +74,7 @@ def default_params(max_ratio: float = 0.8, max_angle: float = 0.7,
     num, den = r * r, 10 ** 8
     g = math.gcd(num, den) if num else den
     return Params(num // g, den // g, n, int(math.ceil(math.cos(max_angle) * n)),
-                  mutual, col_ratio)
+                  mutual, col_ratio, max_features)
 
 
 _lib = None
@@ -152,18 +154,24 @@ class MatchResult:
     col_top2: np.ndarray  # (nB, 4)
 
 
+def _capped(params: Params | None, n: int) -> int:
+    k = (params or Params()).max_features
+    return min(n, k) if k > 0 else n
+
+
 def match(a: np.ndarray, b: np.ndarray, params: Params | None = None) -> MatchResult:
-    """Whole-pair oracle: top-2 tables both ways and the match list."""
+    """Whole-pair oracle: top-2 tables both ways and the match list (under a feature
+    cap K the tables have min(n, K) rows)."""
     a, b = _u8(a), _u8(b)
     p = (params or Params())._c()
-    na, nb = a.shape[0], b.shape[0]
+    na, nb = _capped(params, a.shape[0]), _capped(params, b.shape[0])
     rows = np.zeros((na, 4), np.int32)
     cols = np.zeros((nb, 4), np.int32)
     cap = max(na, 1)  # one match per row at most; min(nA, nB) only with the mutual check
     m = np.zeros((cap, 2), np.int32)
     cnt = np.zeros(1, np.int32)
-    rc = _load().oracle_match(_ptr(a), na, _ptr(b), nb, ctypes.byref(p), _ptr(rows), _ptr(cols),
-                              _ptr(m), cap, _ptr(cnt))
+    rc = _load().oracle_match(_ptr(a), a.shape[0], _ptr(b), b.shape[0], ctypes.byref(p), _ptr(rows),
+                              _ptr(cols), _ptr(m), cap, _ptr(cnt))
     assert rc == 0
     return MatchResult(matches=m[: int(cnt[0])].copy(), row_top2=rows, col_top2=cols)
 

@@ -34,6 +34,12 @@
  *   column direction (ColMatch) feeds the cross check.  Matches are listed by
  *   ascending i.
  *
+ *   Feature cap (the match cap of the "SERAC" page, section "Memory": COLMAP advises
+ *   lowering it when memory is short, and the features past it are clamped away).
+ *   With max_features = K > 0 each image takes part with its first K descriptors
+ *   only, exactly as if the caller had passed n = min(n, K): rows and columns past K
+ *   are neither candidates nor outputs.  K = 0 means no cap.
+ *
  * Parallelism is a plain OpenMP loop over independent rows or columns; every row's
  * (and column's) result is computed by one thread from scratch, so the thread count
  * cannot change a result.
@@ -54,6 +60,7 @@ typedef struct {
   int64_t min_score;    /* distance gate on the best score */
   int32_t mutual;       /* 1: i1(j1(i)) must equal i */
   int32_t col_ratio;    /* 1: column j1(i) must pass the ratio test and gate too */
+  int32_t max_features; /* K > 0: only the first K descriptors of each image; 0: all */
 } oracle_params;
 
 typedef struct {
@@ -186,12 +193,20 @@ static int32_t decide(const oracle_params* p, const oracle_top2* rt, const oracl
   return rt->j1;
 }
 
-/* Whole pair: row and column top-2 tables (either may be NULL), the match list in
- * ascending i (at most `capacity` written) and the total count. */
+/* The number of descriptors of an image of n that take part under the feature cap. */
+static int32_t capped(const oracle_params* p, int32_t n) {
+  return (p->max_features > 0 && n > p->max_features) ? p->max_features : n;
+}
+
+/* Whole pair: row and column top-2 tables (either may be NULL; min(nA, K) and
+ * min(nB, K) entries under a feature cap K), the match list in ascending i (at most
+ * `capacity` written) and the total count. */
 int oracle_match(const uint8_t* A, int32_t nA, const uint8_t* B, int32_t nB,
                  const oracle_params* p, int32_t* row_out, int32_t* col_out,
                  int32_t* matches, int32_t capacity, int32_t* count) {
   if (nA < 0 || nB < 0 || !p || !count) return -1;
+  nA = capped(p, nA);
+  nB = capped(p, nB);
   int32_t* rows = row_out ? row_out : (int32_t*)malloc(sizeof(int32_t) * 4 * (size_t)(nA > 0 ? nA : 1));
   int32_t* cols = col_out ? col_out : (int32_t*)malloc(sizeof(int32_t) * 4 * (size_t)(nB > 0 ? nB : 1));
   if (!rows || !cols) return -2;
@@ -225,6 +240,10 @@ int oracle_accept_rows(const uint8_t* A, int32_t nA, const uint8_t* B, int32_t n
                        const oracle_params* p, const int32_t* rows, int32_t n_rows,
                        int32_t* out_j, int32_t* out_row, int32_t* out_col) {
   if (nA < 0 || nB < 0 || !p || !rows || !out_j) return -1;
+  nA = capped(p, nA);
+  nB = capped(p, nB);
+  for (int32_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= nA) return -1;
   #pragma omp parallel for schedule(dynamic, 1)
   for (int32_t r = 0; r < n_rows; ++r) {
     int32_t i = rows[r];

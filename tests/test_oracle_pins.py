@@ -82,6 +82,35 @@ def test_gate_boundary(oracle_mod, case):
     assert r.matches.tolist() == g["matches_" + case]
 
 
+@pytest.mark.parametrize("case", [0, 1, 2])
+def test_feature_cap(oracle_mod, case):
+    """SERAC page, 'Memory': the match cap clamps away the features past it.  The
+    hand-worked capped 4x4 pair, and the cap against plain truncation of the inputs."""
+    g = _load("feature_cap.json")
+    c = g["cases"][case]
+    vec = {k: _vec(v) for k, v in g["vectors"].items()}
+    A = np.stack([vec[k] for k in g["A"]])
+    B = np.stack([vec[k] for k in g["B"]])
+    r = oracle_mod.match(A, B, oracle_mod.Params(col_ratio=1, max_features=c["max_features"]))
+    assert r.row_top2.tolist() == c["row_top2"]
+    assert r.col_top2.tolist() == c["col_top2"]
+    assert r.matches.tolist() == c["matches_col_ratio_1"]
+    r0 = oracle_mod.match(A, B, oracle_mod.Params(col_ratio=0, max_features=c["max_features"]))
+    assert r0.matches.tolist() == c["matches_col_ratio_0"]
+
+
+def test_feature_cap_is_truncation(oracle_mod):
+    a, b = _tiny_inputs(11, 60, 45, 3)
+    for k in (1, 7, 44, 45, 59, 200):
+        p = oracle_mod.Params(norm_sq=60000, min_score=0, max_features=k)
+        rows, cols, m = _brute(a[:k], b[:k], p)
+        r = oracle_mod.match(a, b, p)
+        assert r.row_top2.tolist() == rows and r.col_top2.tolist() == cols and r.matches.tolist() == m
+        j, rr, _ = oracle_mod.accept_rows(a, b, np.arange(min(k, 60)), p)
+        kept = {i: jj for i, jj in m}
+        assert j.tolist() == [kept.get(i, -1) for i in range(min(k, 60))] and rr.tolist() == rows
+
+
 def test_default_params(oracle_mod):
     p = oracle_mod.default_params(0.8, 0.7)
     assert (p.ratio_num_sq, p.ratio_den_sq) == (16, 25)
