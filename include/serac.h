@@ -64,7 +64,8 @@ extern "C" {
 #define SERAC_EUNSUPPORTED (-6)  /* current device is not sm_103 or TMA encoding unavailable */
 
 /* Matching parameters, exact integers.  serac_default_params fills them from the
- * page's knobs (max_ratio 0.8, max angle 0.7 rad -> 16/25, N = 262144, 200499). */
+ * page's knobs (max_ratio 0.8, max angle 0.7 rad -> 16/25, N = 262144, 200499; no
+ * feature cap). */
 typedef struct {
   int32_t ratio_num_sq; /* r^2 = num / den (0.8 -> 16) */
   int32_t ratio_den_sq; /*                 (0.8 -> 25) */
@@ -72,6 +73,10 @@ typedef struct {
   int32_t min_score;    /* distance gate: s1 >= ceil(cos(max_angle) * N) */
   int32_t mutual;       /* 1: require i1(j1(i)) == i */
   int32_t col_ratio;    /* 1: column j1(i) must pass the same test */
+  int32_t max_features; /* feature cap K ("Memory": the match cap clamps away the
+                           features past it): K > 0 matches only the first K
+                           descriptors of each image, exactly as if the caller had
+                           passed n = min(n, K); 0 = no cap */
 } serac_params;
 
 /* One image pair for match_batch (device pointers, as for match_pair). */
@@ -88,7 +93,9 @@ typedef struct {
  *            first `capacity` were written) or a negative status from the GPU;
  *            capacity n_a always suffices (min(n_a, n_b) when `mutual` is set)
  *   row_top2 optional (NULL to skip): [n_a][4] int32 (s1, j1, s2, j2)
- *   col_top2 optional (NULL to skip): [n_b][4] int32 (c1, i1, c2, i2) */
+ *   col_top2 optional (NULL to skip): [n_b][4] int32 (c1, i1, c2, i2)
+ * Under a feature cap K (serac_params.max_features) read n_a and n_b above as
+ * min(n_a, K) and min(n_b, K): nothing past them is written. */
 typedef struct {
   int32_t* matches;
   int32_t capacity;
@@ -99,7 +106,7 @@ typedef struct {
 
 /* Fill `p` from a ratio (read to 4 decimals, squared and reduced to num/den) and a
  * maximum angle in radians (min_score = ceil(cos(angle) * 262144)); mutual = 1,
- * col_ratio = 1.  Host only.  Returns SERAC_EINVAL if p is NULL, max_ratio is not in
+ * col_ratio = 1, max_features = 0.  Host only.  Returns SERAC_EINVAL if p is NULL, max_ratio is not in
  * (0, 1] or the angle is not in [0, pi/2]. */
 int serac_default_params(serac_params* p, float max_ratio, float max_angle_rad);
 
@@ -138,9 +145,10 @@ int serac_scores(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b, int3
                  int32_t* scores, void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /* Profiling hook: when both events are non-NULL (cudaEvent_t), every following
- * match_pair / match_batch records `ev_begin` just before its fused GEMM + top-2
- * launch and `ev_end` just after it, on the call's stream.  NULL, NULL turns it off.
- * Process-wide setting; not thread-safe. */
+ * match_pair / match_batch call made by the calling thread records `ev_begin` just
+ * before its first fused GEMM + top-2 launch and `ev_end` just after it, on the
+ * call's stream.  NULL, NULL turns it off.  The setting belongs to the calling
+ * thread; other threads' calls are not affected. */
 int serac_set_profile_events(void* ev_begin, void* ev_end);
 
 /* SERAC_OK if the current CUDA device is an sm_103 part this library was built for,
@@ -161,8 +169,8 @@ int serac_last_cuda_error(void);
  * time), the kernel records the timeout in the error word and winds down, and the
  * call reports SERAC_ETIMEOUT through *count; its other outputs are not valid.  No
  * fault, trap or unbounded wait is involved and the context stays usable: the next
- * call runs normally.  The flag is consumed by that one call; enable = 0 clears it.
- * Process-wide, not thread-safe.  Host only; always returns SERAC_OK. */
+ * call runs normally.  The flag belongs to the calling thread and is consumed by its
+ * next call; enable = 0 clears it.  Host only; always returns SERAC_OK. */
 int serac_test_inject_timeout(int enable);
 
 /* Size of the library's built-in scratch used by match_pair_noalloc (16 MiB). */
@@ -177,11 +185,16 @@ int serac_test_inject_timeout(int enable);
  * Scratch is one fixed array of SERAC_NOALLOC_SCRATCH_BYTES inside the library
  * (every GPU that loads the library holds it until the process exits).  The call
  * allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
- *   - Pairs whose serac_pair_workspace_size(n_a, n_b) exceeds the scratch are
- *     rejected with SERAC_EWORKSPACE (pairs up to 16,384 x 16,384 fit).
- *   - The first call on each device looks up the scratch's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call before
- *     any stream capture.
+ *   - n_a or n_b outside 0..SERAC_MAX_N (or a NULL / invalid `params`) gives
+ *     SERAC_EINVAL; pairs whose serac_pair_workspace_size (of the sizes after the
+ *     feature cap) exceeds the scratch are rejected with SERAC_EWORKSPACE (pairs up
+ *     to 16,384 x 16,384 fit).
+ *   - The first call in each CUDA context looks up the scratch's device address
+ *     (cudaGetSymbolAddress) with that context's device current and caches it for
+ *     that context (keyed by the context's unique ID); make that first call before
+ *     any stream capture.  After cudaDeviceReset, or in another context on the same
+ *     device, the module lives at another address: the new context's first call
+ *     looks it up again (so, again, make it before any capture in that context).
  *   - All calls share the one scratch array, which keeps the previous call's
  *     contents (the call clears what must start at zero).  Calls that overlap on the
  *     GPU (other streams, other host threads) race on it: serialise them.
@@ -189,14 +202,17 @@ int serac_test_inject_timeout(int enable);
 int match_pair_noalloc(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b, int32_t n_b,
                        const serac_params* params, const serac_out* out, void* cuda_stream);
 
-/* Host-only view of the work schedule (no GPU needed): for `pairs` (pointers are
- * used only to recognise shared images) and at most `grid` persistent CTAs
- * (1..256), report the number of launch chunks and, for the first chunk, the total
- * number of pieces, the pieces of each pair (out_npieces[pairs of that chunk]; a
- * pair's 128 x 256 tiles are cut into that many runs, one per CTA, 0 for an empty
- * pair) and the tiles each CTA processes (cta_tiles[grid]; CTAs beyond the chunk's
- * launch grid, which has at most one CTA per tile, get 0).  Any output may be NULL.
- * Returns SERAC_EINVAL on bad input. */
+/* Host-only view of the work schedule (no GPU needed).  Every pair is matched as two
+ * row problems -- the rows of A against the columns B, and the rows of B against the
+ * columns A (the pair's column top-2) -- each cut into 128 x 256 tiles.  For `pairs`
+ * (pointers are used only to recognise shared images) and at most `grid` persistent
+ * CTAs (1..256), report the number of launch chunks and, for the first chunk, the
+ * total number of pieces, the pieces of each problem (out_npieces[2 x pairs of that
+ * chunk]: entry 2k for pair k's A rows, 2k + 1 for its B rows; a problem's tiles are
+ * cut into that many runs, one per CTA, 0 for an empty problem) and the tiles each
+ * CTA processes (cta_tiles[grid]; CTAs beyond the chunk's launch grid, which has at
+ * most one CTA per tile, get 0).  Any output may be NULL.  Returns SERAC_EINVAL on
+ * bad input. */
 int serac_schedule_describe(const serac_pair* pairs, int32_t n_pairs, int32_t grid, int32_t* out_chunks,
                             int32_t* out_pieces, int32_t* out_npieces, int32_t* cta_tiles);
 

@@ -90,44 +90,94 @@ def test_bad_arguments_rejected_before_any_launch(serac):
     assert L.match_batch(None, -1, ctypes.byref(p), None, 256, ws, None) == serac.EINVAL
 
 
+def test_noalloc_argument_checks(serac):
+    """match_pair_noalloc rejects bad sizes before any CUDA call: out of range -> EINVAL,
+    a workspace larger than the built-in scratch (after the feature cap) -> EWORKSPACE."""
+    L = serac.lib()
+    p = serac.default_params()
+    cnt = ctypes.c_int32()
+    out = serac._Out(16, 4, ctypes.addressof(cnt), None, None)
+    assert L.match_pair_noalloc(16, -1, 16, 4, ctypes.byref(p), ctypes.byref(out), None) == serac.EINVAL
+    assert L.match_pair_noalloc(16, (1 << 24) + 1, 16, 4, ctypes.byref(p), ctypes.byref(out), None) == serac.EINVAL
+    assert L.match_pair_noalloc(16, 4, 16, 4, None, ctypes.byref(out), None) == serac.EINVAL
+    big = 32768
+    assert serac.pair_workspace_size(big, big) > serac.NOALLOC_SCRATCH_BYTES
+    assert L.match_pair_noalloc(16, big, 32, big, ctypes.byref(p), ctypes.byref(out), None) == serac.EWORKSPACE
+    p.max_features = -1
+    assert L.match_pair_noalloc(16, 4, 16, 4, ctypes.byref(p), ctypes.byref(out), None) == serac.EINVAL
+
+
+def test_feature_cap_params(serac):
+    """max_features: 0 by default, negative rejected before any launch."""
+    L = serac.lib()
+    p = serac.default_params()
+    assert p.max_features == 0
+    assert serac.default_params(max_features=500).max_features == 500
+    cnt = ctypes.c_int32()
+    out = serac._Out(16, 4, ctypes.addressof(cnt), None, None)
+    p.max_features = -3
+    assert L.match_pair(16, 4, 16, 4, ctypes.byref(p), ctypes.byref(out), 256, 1 << 20, None) == serac.EINVAL
+    assert L.match_batch(None, 0, ctypes.byref(p), None, 256, 1 << 20, None) == serac.EINVAL
+
+
+def test_default_params_agree_with_the_oracle(serac, oracle_mod):
+    """The library's integer parameters and the oracle's, derived separately from the
+    same ratio and angle, agree (including non-default ratios and angles)."""
+    for r, ang in [(0.8, 0.7), (0.7, 0.6), (0.9, 0.8), (0.75, 0.5), (1.0, 1.2), (0.6, 0.0)]:
+        p = serac.default_params(r, ang)
+        q = oracle_mod.default_params(r, ang)
+        assert (p.ratio_num_sq, p.ratio_den_sq, p.norm_sq, p.min_score) == \
+            (q.ratio_num_sq, q.ratio_den_sq, q.norm_sq, q.min_score), (r, ang)
+
+
 def _tiles(na, nb):
+    """Tiles of one row problem: 128-row tiles of the row side, 256-row tiles of the other."""
     return ((na + 127) // 128) * ((nb + 255) // 256) if na > 0 and nb > 0 else 0
 
 
+def _pair_tiles(na, nb):
+    """A pair is two row problems: A's rows against B, B's rows against A."""
+    return _tiles(na, nb) + _tiles(nb, na)
+
+
 def test_schedule_covers_every_tile_once(serac):
-    # a single 8192 x 8192 pair on 152 CTAs: 2048 tiles dealt 13 or 14 per CTA
+    # a single 8192 x 8192 pair on 152 CTAs: 2 x 2048 tiles dealt 26 or 27 per CTA
     chunks, pieces, npieces, cta = serac.schedule_describe([(8192, 8192)], 152)
     assert chunks == 1
-    assert npieces == [152] and pieces == 152
-    assert sum(cta) == 64 * 32
-    assert sorted(set(cta)) == [13, 14] and cta.count(14) == 2048 % 152
+    assert npieces == [152, 152] and pieces == 304
+    assert sum(cta) == 2 * 64 * 32
+    assert sorted(set(cta)) == [26, 27] and cta.count(27) == 4096 % 152
 
 
-def test_schedule_small_pair_uses_fewer_ctas(serac):
-    # 2000 x 2000: 16 x 8 = 128 tiles, one per CTA; the other 24 CTAs are not launched
+def test_schedule_small_pair_uses_every_cta(serac):
+    # 2000 x 2000: two problems of 16 x 8 = 128 tiles; 152 CTAs take one or two tiles
     chunks, pieces, npieces, cta = serac.schedule_describe([(2000, 2000)], 152)
-    assert npieces == [128] and pieces == 128
-    assert cta[:128] == [1] * 128 and cta[128:] == [0] * 24
+    assert npieces == [128, 128] and pieces == 256
+    assert sum(cta) == 256 and sorted(set(cta)) == [1, 2]
+    # a pair with fewer tiles than CTAs launches one CTA per tile
+    chunks, pieces, npieces, cta = serac.schedule_describe([(300, 500)], 152)
+    assert npieces == [_tiles(300, 500), _tiles(500, 300)] and sum(cta) == sum(npieces)
+    assert cta[:sum(npieces)] == [1] * sum(npieces) and set(cta[sum(npieces):]) == {0}
 
 
 def test_schedule_ragged_and_empty(serac):
     sizes = [(1000, 16384), (0, 500), (257, 0), (129, 255), (16384, 1000)]
     chunks, pieces, npieces, cta = serac.schedule_describe(sizes, 152)
-    t = [_tiles(na, nb) for na, nb in sizes]
+    t = [x for na, nb in sizes for x in (_tiles(na, nb), _tiles(nb, na))]
     assert npieces == [min(152, x) for x in t]
-    assert npieces[1] == 0 and npieces[2] == 0
+    assert npieces[2:6] == [0, 0, 0, 0]
     assert pieces == sum(npieces)
     assert sum(cta) == sum(t)
-    # tiles are dealt round-robin across pairs: loads differ by at most one
+    # tiles are dealt round-robin across problems: loads differ by at most one
     assert max(cta) - min(cta) <= 1
 
 
 def test_schedule_balanced_over_many_pairs(serac):
-    # 40 pairs of 1,700 tiles and 40 of 5 tiles: every CTA within one tile of the mean
+    # 40 pairs of 1,700 + 1,700 tiles and 40 of 5 + 6 tiles: every CTA within one tile
     sizes = [(6400, 8704), (640, 256)] * 40
     chunks, pieces, npieces, cta = serac.schedule_describe(sizes, 152)
     assert chunks == 1
-    total = sum(_tiles(na, nb) for na, nb in sizes)
+    total = sum(_pair_tiles(na, nb) for na, nb in sizes)
     assert sum(cta) == total
     assert max(cta) - min(cta) <= 1
 
@@ -137,8 +187,8 @@ def test_schedule_large_batch_chunks(serac):
     chunks, pieces, npieces, cta = serac.schedule_describe(sizes, 152)
     # at most 128 pairs per launch chunk (their tables travel as kernel parameters)
     assert chunks == 3
-    assert npieces[0] == 152 and pieces == 128 * 152
-    assert sum(cta) == 128 * 2048 and max(cta) - min(cta) <= 1
+    assert npieces[0] == 152 and pieces == 2 * 128 * 152
+    assert sum(cta) == 128 * 2 * 2048 and max(cta) - min(cta) <= 1
 
 
 def test_timeout_hook_is_host_only(serac):

@@ -41,7 +41,8 @@ class SeracError(RuntimeError):
 class Params(ctypes.Structure):
     _fields_ = [("ratio_num_sq", ctypes.c_int32), ("ratio_den_sq", ctypes.c_int32),
                 ("norm_sq", ctypes.c_int32), ("min_score", ctypes.c_int32),
-                ("mutual", ctypes.c_int32), ("col_ratio", ctypes.c_int32)]
+                ("mutual", ctypes.c_int32), ("col_ratio", ctypes.c_int32),
+                ("max_features", ctypes.c_int32)]
 
     def __repr__(self):
         return ("Params(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")")
@@ -98,11 +99,17 @@ def _check(status: int, what: str) -> None:
 
 
 def default_params(max_ratio: float = 0.8, max_angle: float = 0.7, mutual: int = 1,
-                   col_ratio: int = 1) -> Params:
+                   col_ratio: int = 1, max_features: int = 0) -> Params:
+    """Integer test parameters from the ratio and the maximum angle (serac_default_params);
+    max_features = K > 0 matches only the first K descriptors of each image."""
     p = Params()
     _check(lib().serac_default_params(ctypes.byref(p), max_ratio, max_angle), "serac_default_params")
-    p.mutual, p.col_ratio = int(mutual), int(col_ratio)
+    p.mutual, p.col_ratio, p.max_features = int(mutual), int(col_ratio), int(max_features)
     return p
+
+
+def _capped(p: Params, n: int) -> int:
+    return min(n, p.max_features) if p.max_features > 0 else n
 
 
 def device_check() -> int:
@@ -216,7 +223,7 @@ def match_pair(a: torch.Tensor, b: torch.Tensor, params: Optional[Params] = None
     if out is not None:
         o, c = out, output_for(out)
     else:
-        o, c = _make_out(n_a, n_b, dev, capacity, top2, host=host_out)
+        o, c = _make_out(_capped(p, n_a), _capped(p, n_b), dev, capacity, top2, host=host_out)
     st = lib().match_pair(a.data_ptr(), n_a, b.data_ptr(), n_b, ctypes.byref(p), ctypes.byref(c),
                           ws.data_ptr(), ws.numel(), _stream_ptr(stream))
     _check(st, "match_pair")
@@ -230,7 +237,7 @@ def match_pair_noalloc(a: torch.Tensor, b: torch.Tensor, params: Optional[Params
     caller's.  Calls sharing the scratch must not overlap on the GPU."""
     a, b = _desc(a, "a"), _desc(b, "b")
     p = params if params is not None else default_params()
-    o, c = _make_out(a.shape[0], b.shape[0], a.device, capacity, top2)
+    o, c = _make_out(_capped(p, a.shape[0]), _capped(p, b.shape[0]), a.device, capacity, top2)
     st = lib().match_pair_noalloc(a.data_ptr(), a.shape[0], b.data_ptr(), b.shape[0], ctypes.byref(p),
                                   ctypes.byref(c), _stream_ptr(stream))
     _check(st, "match_pair_noalloc")
@@ -278,7 +285,7 @@ def match_batch(pairs: Sequence, params: Optional[Params] = None, *, capacities=
             o, c = outs[k], output_for(outs[k])
         else:
             cap = None if capacities is None else capacities[k]
-            o, c = _make_out(a.shape[0], b.shape[0], dev, cap, top2, host=host_out)
+            o, c = _make_out(_capped(p, a.shape[0]), _capped(p, b.shape[0]), dev, cap, top2, host=host_out)
         res.append(o)
         couts[k] = c
     st = lib().match_batch(arr, n, ctypes.byref(p), couts, ws.data_ptr(), ws.numel(), _stream_ptr(stream))
@@ -317,16 +324,53 @@ def shard_pairs(sizes: Sequence, world: int) -> list:
     return [sorted(x) for x in shards]
 
 
+def match_batch_shard(pairs: Sequence, rank: int, world: int, params: Optional[Params] = None, **kwargs):
+    """One GPU's share of a sharded batch: the pairs shard_pairs() gives `rank` of
+    `world`, matched by one match_batch on the current device.  Returns (indices of
+    those pairs in `pairs`, their MatchOutputs).  Nothing crosses ranks here; see
+    gather_matches for collecting the lists afterwards."""
+    sizes = [(int(a.shape[0]), int(b.shape[0])) for a, b in pairs]
+    mine = shard_pairs(sizes, world)[rank]
+    outs = match_batch([pairs[k] for k in mine], params, **kwargs) if mine else []
+    return mine, outs
+
+
+def gather_matches(mine: Sequence, outs: Sequence, n_pairs: int, group=None, dst: int = 0):
+    """Collect the match lists of a sharded batch on rank `dst` after every rank has run
+    its match_batch_shard: returns, on `dst`, the list of all n_pairs (count, 2) int32
+    CPU tensors in the batch's pair order, and None on the other ranks.  A host-side
+    collection (torch.distributed.gather_object over the process group), after the
+    GPU work; the matching itself has no collective."""
+    import torch.distributed as dist
+    local = [(int(k), o.result()) for k, o in zip(mine, outs)]
+    rank = dist.get_rank(group)
+    parts = [None] * dist.get_world_size(group) if rank == dst else None
+    dist.gather_object(local, parts, dst=dst, group=group)
+    if rank != dst:
+        return None
+    res = [None] * n_pairs
+    for part in parts:
+        for k, m in part:
+            if res[k] is not None:
+                raise RuntimeError(f"pair {k} came from two ranks")
+            res[k] = m
+    missing = [k for k, m in enumerate(res) if m is None]
+    if missing:
+        raise RuntimeError(f"pairs {missing[:8]} came from no rank")
+    return res
+
+
 def schedule_describe(sizes: Sequence, grid: int):
     """Host-side view of how the first launch chunk of pairs with these (n_a, n_b)
-    sizes is cut: (chunks, pieces, pieces per pair, tiles per CTA[grid])."""
+    sizes is cut: (chunks, pieces, pieces per row problem -- two per pair: A's rows,
+    then B's rows --, tiles per CTA[grid])."""
     n = len(sizes)
     arr = (_Pair * max(n, 1))()
     for k, (na, nb) in enumerate(sizes):
         arr[k] = _Pair(16 * (2 * k + 1), int(na), 16 * (2 * k + 2), int(nb))
     chunks, pieces = ctypes.c_int32(), ctypes.c_int32()
-    npieces = (ctypes.c_int32 * max(n, 1))()
+    npieces = (ctypes.c_int32 * max(2 * n, 1))()
     cta_tiles = (ctypes.c_int32 * grid)()
     _check(lib().serac_schedule_describe(arr, n, grid, ctypes.byref(chunks), ctypes.byref(pieces),
                                          npieces, cta_tiles), "serac_schedule_describe")
-    return chunks.value, pieces.value, list(npieces)[:n], list(cta_tiles)
+    return chunks.value, pieces.value, list(npieces)[:2 * n], list(cta_tiles)

@@ -1,13 +1,16 @@
 // C ABI of libserac_gb300: argument checks, image staging plan, workspace layout,
 // the work schedule of the persistent fused kernel, and the launch sequence.
 //
-// Schedule.  Pairs are processed in launch chunks of at most MAX_PAIRS pairs (the
-// per-pair tables travel as kernel parameters, so a call needs no host-to-device
-// copy and can be captured in a CUDA graph).  Within a chunk every pair's tiles are
-// cut into as many pieces as there are persistent CTAs (fewer for small pairs), one
-// piece per CTA, with the CTA of a pair's first piece rotating from pair to pair so
-// that the CTAs' tile counts stay within one tile per pair of each other; every CTA
-// walks the pairs in the same order, so the pairs in flight share L2.
+// Schedule.  Every pair is two row problems for the fused kernel: the rows of A
+// against the columns B (its row top-2) and the rows of B against the columns A (its
+// column top-2).  Pairs are processed in launch chunks of at most MAX_PAIRS pairs (the
+// per-problem tables travel as kernel parameters, so a call needs no host-to-device
+// copy and can be captured in a CUDA graph).  Within a chunk every problem's tiles are
+// cut into as many pieces as there are persistent CTAs (fewer for small problems), one
+// piece per CTA, with the CTA of a problem's first piece rotating from problem to
+// problem so that the CTAs' tile counts stay within one tile per problem of each
+// other; every CTA walks the problems in the same order, so the pairs in flight share
+// L2.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -32,7 +35,7 @@ size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 struct Chunk {
   int p0 = 0, p1 = 0;          // pairs [p0, p1)
   int img0 = 0, img1 = 0;      // images first used by this chunk: [img0, img1)
-  int64_t tiles = 0;           // 128 x 256 tiles of all its pairs
+  int64_t tiles = 0;           // 128 x 256 tiles of all its problems (two per pair)
   int64_t rows = 0, cols = 0;  // sum of n_a, n_b
   int64_t blocks = 0;          // match-kernel blocks
 };
@@ -53,9 +56,20 @@ int64_t col_tiles(int32_t n_b) { return (static_cast<int64_t>(n_b) + BN - 1) / B
 
 int64_t match_blocks(int32_t n_a) { return std::max<int64_t>(1, (static_cast<int64_t>(n_a) + MATCH_ROWS_PER_BLOCK - 1) / MATCH_ROWS_PER_BLOCK); }
 
-int64_t pair_tiles(const serac_pair& pr) {
-  if (pr.n_a <= 0 || pr.n_b <= 0) return 0;
-  return row_tiles(pr.n_a) * col_tiles(pr.n_b);
+// Tiles of the row problem of n_rows rows against n_cols columns.
+int64_t problem_tiles(int32_t n_rows, int32_t n_cols) {
+  if (n_rows <= 0 || n_cols <= 0) return 0;
+  return row_tiles(n_rows) * col_tiles(n_cols);
+}
+
+// Tiles of a pair: its rows against B's descriptors, and B's rows against A's.
+int64_t pair_tiles(const serac_pair& pr) { return problem_tiles(pr.n_a, pr.n_b) + problem_tiles(pr.n_b, pr.n_a); }
+
+// Tiles of problem 2k (orientation 0: A's rows) or 2k + 1 (orientation 1: B's rows) of
+// the pairs [p0, p1).
+int64_t chunk_problem_tiles(const serac_pair* pairs, int p0, int problem) {
+  const serac_pair& pr = pairs[p0 + problem / 2];
+  return (problem & 1) ? problem_tiles(pr.n_b, pr.n_a) : problem_tiles(pr.n_a, pr.n_b);
 }
 
 void build_plan(const serac_pair* pairs, int32_t n_pairs, Plan& pl) {
@@ -143,15 +157,16 @@ int chunk_grid(const Chunk& ch, int sms) {
 // more for the first T mod grid pieces.
 int64_t piece_tiles(int64_t t, int grid, int k) { return t / grid + (k < t % grid ? 1 : 0); }
 
-// Pieces per pair (min(grid, tiles)) and the CTA of each pair's first piece.  The
-// pieces that carry one tile more go to the CTAs after those that took the previous
-// pair's, so over a chunk every CTA gets the same number of tiles within one.
+// Pieces per problem (min(grid, tiles)) and the CTA of each problem's first piece,
+// for the 2 (p1 - p0) problems of a chunk.  The pieces that carry one tile more go to
+// the CTAs after those that took the previous problem's, so over a chunk every CTA gets
+// the same number of tiles within one.
 void plan_pieces(const serac_pair* pairs, const Chunk& ch, int grid, int32_t* npieces, int32_t* offset) {
   int off = 0;
-  for (int k = ch.p0; k < ch.p1; ++k) {
-    const int64_t t = pair_tiles(pairs[k]);
-    npieces[k - ch.p0] = static_cast<int>(std::min<int64_t>(grid, t));
-    offset[k - ch.p0] = off;
+  for (int k = 0; k < 2 * (ch.p1 - ch.p0); ++k) {
+    const int64_t t = chunk_problem_tiles(pairs, ch.p0, k);
+    npieces[k] = static_cast<int>(std::min<int64_t>(grid, t));
+    offset[k] = off;
     off = static_cast<int>((off + t % grid) % grid);
   }
 }
@@ -218,7 +233,8 @@ int encode_staged_map(CUtensorMap* map, void* staged, int64_t rows) {
   return r == CUDA_SUCCESS ? SERAC_OK : SERAC_ECUDA;
 }
 
-cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
+// profiling events of the calling thread's calls (serac_set_profile_events)
+thread_local cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
 
 // Per host thread and device: a side stream on which match_batch stages the images of
 // its later launch chunks while the earlier chunks compute, and the events that order
@@ -251,7 +267,7 @@ int side_stream(size_t n_events, SideStream** out) {
   *out = &s;
   return SERAC_OK;
 }
-bool g_inject_no_copies = false;  // consumed by the next call's first fused launch
+thread_local bool g_inject_no_copies = false;  // consumed by this thread's next call
 thread_local int g_last_launches = 0;    // per calling thread
 thread_local int g_last_cuda_error = 0;
 
@@ -270,8 +286,13 @@ int check_pairs(const serac_pair* pairs, int32_t n_pairs) {
 
 int check_params(const serac_params* p) {
   if (!p) return SERAC_EINVAL;
-  if (p->ratio_num_sq < 0 || p->ratio_den_sq <= 0) return SERAC_EINVAL;
+  if (p->ratio_num_sq < 0 || p->ratio_den_sq <= 0 || p->max_features < 0) return SERAC_EINVAL;
   return SERAC_OK;
+}
+
+// Descriptors of an image of n that take part under the feature cap: the first K.
+int32_t capped(const serac_params* p, int32_t n) {
+  return (p->max_features > 0 && n > p->max_features) ? p->max_features : n;
 }
 
 int check_out(const serac_out* o, int32_t n_a, int32_t n_b) {
@@ -370,15 +391,13 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
     unsigned long long* colkeys = reinterpret_cast<unsigned long long*>(region + pl.r_colkeys);
     // this chunk's images (staged on the side stream) must be in place
     if (on_side[ci]) SERAC_TRY_CUDA(cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), side->staged[ci], 0));
-    // ---------------- fused GEMM + top-2, merged into the key arrays
+    // ---------------- fused GEMM + row top-2 of both problems of every pair
     if (ch.tiles > 0) {
       FusedParams fp;
       std::memset(&fp, 0, sizeof(fp));
       fp.grid = chunk_grid(ch, sms);
-      int32_t npieces[MAX_PAIRS], offset[MAX_PAIRS];
+      int32_t npieces[MAX_PROBLEMS], offset[MAX_PROBLEMS];
       plan_pieces(pairs, ch, fp.grid, npieces, offset);
-      fp.rowkeys = rowkeys;
-      fp.colkeys = colkeys;
       fp.err = err;
       fp.dump = dump;
       fp.dump_ld = (dump && n_pairs > 0) ? pairs[0].n_b : 0;
@@ -393,16 +412,19 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
       int np = 0;
       int64_t rows = 0, cols = 0;
       for (int k = ch.p0; k < ch.p1; ++k) {
-        if (npieces[k - ch.p0] > 0) {
+        const int32_t ra = pl.images[pl.a_img[k]].row0, rb = pl.images[pl.b_img[k]].row0;
+        for (int o = 0; o < 2; ++o) {
+          const int pi = 2 * (k - ch.p0) + o;
+          if (npieces[pi] == 0) continue;
           FusedPair& f = fp.pairs[np++];
-          f.a_row0 = pl.images[pl.a_img[k]].row0;
-          f.b_row0 = pl.images[pl.b_img[k]].row0;
-          f.n_a = pairs[k].n_a;
-          f.n_b = pairs[k].n_b;
-          f.npieces = npieces[k - ch.p0];
-          f.offset = offset[k - ch.p0];
-          f.row_base = static_cast<int32_t>(rows);
-          f.col_base = static_cast<int32_t>(cols);
+          f.a_row0 = o ? rb : ra;
+          f.b_row0 = o ? ra : rb;
+          f.n_a = o ? pairs[k].n_b : pairs[k].n_a;
+          f.n_b = o ? pairs[k].n_a : pairs[k].n_b;
+          f.npieces = npieces[pi];
+          f.offset = offset[pi];
+          f.transposed = o;
+          f.keys = o ? colkeys + 2 * cols : rowkeys + 2 * rows;
         }
         rows += pairs[k].n_a;
         cols += pairs[k].n_b;
@@ -457,10 +479,6 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
     }
     fn.n_pairs = np;
     fn.total_blocks = static_cast<int32_t>(blocks);
-    // a grid of at most one block per SM has every block resident once the fused
-    // kernel is done, so blocks may take their order from the block index (no ticket
-    // round trip); larger grids keep the tickets (a block only waits on started ones)
-    fn.index_order = blocks <= sms ? 1 : 0;
     if (np > 0) {
       SERAC_TRY_CUDA(static_cast<cudaError_t>(launch_match(fn, stream)));
       ++g_last_launches;
@@ -497,6 +515,7 @@ int serac_default_params(serac_params* p, float max_ratio, float max_angle_rad) 
   p->min_score = static_cast<int32_t>(std::ceil(std::cos(static_cast<double>(max_angle_rad)) * n));
   p->mutual = 1;
   p->col_ratio = 1;
+  p->max_features = 0;
   return SERAC_OK;
 }
 
@@ -530,6 +549,8 @@ int match_pair(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b, int32_
   if (st == SERAC_OK) st = check_params(params);
   if (st == SERAC_OK) st = check_out(out, n_a, n_b);
   if (st != SERAC_OK) return st;
+  pr.n_a = capped(params, n_a);
+  pr.n_b = capped(params, n_b);
   return run(&pr, 1, params, out, nullptr, workspace, workspace_bytes, cuda_stream);
 }
 
@@ -543,7 +564,14 @@ int match_batch(const serac_pair* pairs, int32_t n_pairs, const serac_params* pa
     st = check_out(&outs[p], pairs[p].n_a, pairs[p].n_b);
     if (st != SERAC_OK) return st;
   }
-  return run(pairs, n_pairs, params, outs, nullptr, workspace, workspace_bytes, cuda_stream);
+  if (params->max_features == 0)
+    return run(pairs, n_pairs, params, outs, nullptr, workspace, workspace_bytes, cuda_stream);
+  std::vector<serac_pair> cp(pairs, pairs + n_pairs);
+  for (serac_pair& pr : cp) {
+    pr.n_a = capped(params, pr.n_a);
+    pr.n_b = capped(params, pr.n_b);
+  }
+  return run(cp.data(), n_pairs, params, outs, nullptr, workspace, workspace_bytes, cuda_stream);
 }
 
 int serac_scores(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b, int32_t n_b, int32_t* scores,
@@ -590,19 +618,19 @@ int serac_schedule_describe(const serac_pair* pairs, int32_t n_pairs, int32_t gr
   if (out_chunks) *out_chunks = static_cast<int32_t>(pl.chunks.size());
   const Chunk& ch = pl.chunks.front();
   const int g = chunk_grid(ch, grid);
-  int32_t npieces[MAX_PAIRS], offset[MAX_PAIRS];
+  int32_t npieces[MAX_PROBLEMS], offset[MAX_PROBLEMS];
   plan_pieces(pairs, ch, g, npieces, offset);
+  const int nprob = 2 * (ch.p1 - ch.p0);
   int64_t total = 0;
-  for (int k = ch.p0; k < ch.p1; ++k) total += npieces[k - ch.p0];
+  for (int k = 0; k < nprob; ++k) total += npieces[k];
   if (out_pieces) *out_pieces = static_cast<int32_t>(total);
   if (out_npieces)
-    for (int k = ch.p0; k < ch.p1; ++k) out_npieces[k - ch.p0] = npieces[k - ch.p0];
+    for (int k = 0; k < nprob; ++k) out_npieces[k] = npieces[k];
   if (cta_tiles) {
     for (int c = 0; c < grid; ++c) cta_tiles[c] = 0;
-    for (int k = ch.p0; k < ch.p1; ++k) {
-      const int64_t t = pair_tiles(pairs[k]);
-      for (int i = 0; i < npieces[k - ch.p0]; ++i)
-        cta_tiles[(offset[k - ch.p0] + i) % g] += static_cast<int32_t>(piece_tiles(t, g, i));
+    for (int k = 0; k < nprob; ++k) {
+      const int64_t t = chunk_problem_tiles(pairs, ch.p0, k);
+      for (int i = 0; i < npieces[k]; ++i) cta_tiles[(offset[k] + i) % g] += static_cast<int32_t>(piece_tiles(t, g, i));
     }
   }
   return SERAC_OK;

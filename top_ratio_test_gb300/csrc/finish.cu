@@ -103,16 +103,12 @@ __global__ void __launch_bounds__(MATCH_THREADS, 65536 / (MATCH_THREADS * 32)) m
   __shared__ int s_b, s_prefix;
   __shared__ int warp_off[MATCH_THREADS / 32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  // block order within the pair: the block index when the whole grid is resident at
-  // once, else a ticket, so that a block only ever waits on blocks that have started
-  int b;
-  if (P.index_order) {
-    b = static_cast<int>(blockIdx.x) - fp.blk_base;
-  } else {
-    if (threadIdx.x == 0) s_b = atomicAdd(&P.tickets[lo], 1);
-    __syncthreads();
-    b = s_b;
-  }
+  // block order within the pair: a ticket, taken by the block once it runs, so that a
+  // block only ever waits on blocks that already hold a ticket and are running --
+  // whatever else shares the GPU and whichever blocks it keeps from being scheduled
+  if (threadIdx.x == 0) s_b = atomicAdd(&P.tickets[lo], 1);
+  __syncthreads();
+  const int b = s_b;
 
   const int ib = b * MATCH_ROWS_PER_BLOCK + static_cast<int>(threadIdx.x) * MATCH_ROWS_PER_THREAD;
   int4 rt[MATCH_ROWS_PER_THREAD];

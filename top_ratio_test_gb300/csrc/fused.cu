@@ -1,42 +1,41 @@
-// Fused similarity contraction + row/column top-2 for exhaustive SIFT matching.
+// Fused similarity contraction + row top-2 for exhaustive SIFT matching.
 //
 // The "SERAC" page ("What changed": DP4A, fused row reduction, wider tiles) keeps
 // the best two scores of each row in registers while the dot products are formed,
-// so the num1 x num2 matrix is never written, and reduces the column direction from
-// per-block partials for the cross check.  This kernel keeps that dataflow but forms
-// the dot products on the sm_103a tensor cores instead of DP4A:
+// so the num1 x num2 matrix is never written.  This kernel keeps that dataflow but
+// forms the dot products on the sm_103a tensor cores instead of DP4A, and it does so
+// for row problems only: the column top-2 of a pair (A, B) is the row top-2 of
+// (B, A), so the host hands every pair over as two problems, and both directions of
+// the match come out of the same in-thread reduction:
 //
 //   * a persistent CTA per SM takes one contiguous piece (a row-major run of
-//     128 x 256 tiles) of every pair of the launch; the tiles of a piece on one row
-//     tile form a segment: one 128-row tile of A resident in shared memory against a
-//     run of 256-row tiles of B streamed by TMA (128-byte swizzle, two stages);
+//     128 x 256 tiles) of every problem of the launch; the tiles of a piece on one
+//     row tile form a segment: one 128-row tile resident in shared memory against a
+//     run of 256-row column tiles streamed by TMA (128-byte swizzle, two stages);
 //   * one thread issues tcgen05.mma kind::f16 (bf16 x bf16 -> f32, M=128, N=256,
 //     K=16 x 8) into one of two TMEM accumulators (2 x 256 columns), so the epilogue
 //     of tile t overlaps the MMAs of tile t+1.  u8 values are exact in bf16 and every
 //     partial sum is an integer below 2^24, so the f32 accumulator holds the exact
 //     integer score ("Exactness": 128 * 255^2 = 8,323,200 cannot overflow);
 //   * sixteen epilogue warps (four per SM sub-partition) read the accumulator
-//     (thread = row, 64 columns each) and
+//     (thread = row, 64 columns each, one 64-column TMEM load per tile) and
 //       - read 2^23 + s (each tile's first MMA writes 2^23 from two small bias
 //         operands), whose f32 bits are the integer 0x4B000000 | s,
-//       - build packed keys s << 8 | index with one integer operation each (the
-//         shift by 8 drops the exponent bits), so a plain max orders by
-//         score then lower index -- the order-independent tie rule of "Real-Time
-//         Dense Stereo at 34 Hz on a Jetson TX2 (MASDA, Part 3)", section 6, which
-//         packs (value, k) into one integer for its fused warp top-2.  Every key is
-//         below 0x7F800000, so keys also compare correctly as finite floats and the
-//         3-input float max can merge them;
-//       - reduce each 16-key sub-chunk with a tree (for instruction-level parallelism)
-//         and keep the row top-2 in registers across the segment,
-//       - take the top-2 of every column over the warp's 32 rows with two warp-wide
-//         max reductions per column (the second as the max of key - best, which
-//         wraps the best to 0), merge the four row quadrants in shared memory, and
-//         fold the tile's column top-2 into the column's global top-2 with 64-bit
-//         atomicMax ("Wider tiles": the column partials, here merged in place).
+//       - build packed keys s << 8 | index with one integer multiply-add each (the
+//         multiply by 256 drops the exponent bits), so a plain max orders by score
+//         then lower index -- the order-independent tie rule of "Real-Time Dense
+//         Stereo at 34 Hz on a Jetson TX2 (MASDA, Part 3)", section 6, which packs
+//         (value, k) into one integer for its fused warp top-2.  Every key is below
+//         0x7F800000, so keys also compare correctly as finite floats and the 3-input
+//         float max can merge them;
+//       - reduce each 32-key half with a min/max tree and keep each row's top-2 in
+//         registers across the segment;
+//     no epilogue warp waits for another: they share only the accumulator barriers.
 //
-// Global top-2 by atomics: old = max(best, x1); second = max(second, min(old, x1));
-// second = max(second, x2).  Every candidate other than the final best reaches
-// `second`, the final best never does (keys are unique), whatever the order.
+// Global top-2 by atomics at the end of a segment: old = max(best, x1);
+// second = max(second, min(old, x1)); second = max(second, x2).  Every candidate other
+// than the final best reaches `second`, the final best never does (keys are unique),
+// whatever the order.
 //
 // Zero-padded rows and columns score 0 and fall to the zero floor, so ragged tails
 // need no masking.  Every wait is bounded; a timeout sets an error bit that the
@@ -62,9 +61,7 @@ constexpr int NUM_EPI_WARPS = 16;
 
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + A_BYTES;
-constexpr int OFF_M = OFF_B + 2 * B_BYTES;
-constexpr int M_BYTES = 2 * 4 * BN * 8;  // [parity][quadrant][column] (k1, k2 - k1 mod 2^32)
-constexpr int OFF_BAR = OFF_M + M_BYTES;
+constexpr int OFF_BAR = OFF_B + 2 * B_BYTES;
 constexpr int BAR_BYTES = 256;
 // bias operands of the first MMA of every tile (no swizzle, one 8-row group read by
 // every group): A_bias rows [1, 0, ..., 0], B_bias rows [2^23, 0, ..., 0], each two K
@@ -78,21 +75,21 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
-// Where a CTA stands in its work: pair p, the next tile t of its piece of that pair
-// and the piece's end (tiles numbered row-major within the pair).
+// Where a CTA stands in its work: problem p, the next tile t of its piece of that
+// problem and the piece's end (tiles numbered row-major within the problem).
 struct Cursor {
   int p, t, tend;
 };
 
-// One segment: row tile rt of pair p against the column tiles [ct0, ct1).
+// One segment: row tile rt of problem p against the column tiles [ct0, ct1).
 struct Segment {
   int p, rt, ct0, ct1;
 };
 
 // Advances `cur` by one segment; false once the CTA has no work left.  Piece k of a
-// pair belongs to CTA (offset + k) mod grid: the pair's T tiles are dealt as q = T / grid
-// tiles per piece plus one more for the first r = T mod grid pieces, so piece k starts
-// at tile k q + min(k, r).
+// problem belongs to CTA (offset + k) mod grid: the problem's T tiles are dealt as
+// q = T / grid tiles per piece plus one more for the first r = T mod grid pieces, so
+// piece k starts at tile k q + min(k, r).
 __device__ __forceinline__ bool next_segment(const FusedParams& P, Cursor& cur, Segment& g) {
   while (cur.t >= cur.tend) {
     if (++cur.p >= P.n_pairs) return false;
@@ -153,11 +150,6 @@ __device__ __forceinline__ void tree_top2(const float (&x)[N], float& k1, float&
   }
   k1 = hi[0];
   k2 = lo[0];
-}
-__device__ __forceinline__ void ins2_64(unsigned long long& k1, unsigned long long& k2, unsigned long long x) {
-  if (x > k2) {
-    if (x > k1) { k2 = k1; k1 = x; } else { k2 = x; }
-  }
 }
 // 32-bit key s << 8 | (255 - local) -> 64-bit s << 32 | ~(base + local); 0 if s == 0.
 __device__ __forceinline__ unsigned long long key64(uint32_t k, uint32_t base) {
@@ -318,21 +310,16 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     const int q = warp & 3;       // TMEM lane quadrant this warp may read
     const int qt = e >> 2;        // which 64-column quarter of the tile
     const uint32_t rl = static_cast<uint32_t>(q * 32 + lane);  // row within the tile
-    const uint32_t col_low = 255u - rl;                         // column keys carry the row
-    // keys are u * 256 + index bits (the multiply shifts the exponent bits out).  Both
-    // take 256 from a kernel parameter so that the compiler keeps them one integer
-    // multiply-add each on the FMA pipe: the min/max trees keep the ALU pipe busy
+    // keys are u * 256 + index bits (the multiply shifts the exponent bits out); 256
+    // comes from a kernel parameter so that the compiler keeps each key one integer
+    // multiply-add on the FMA pipe while the min/max trees keep the ALU pipe busy
     const uint32_t key_mult = P.key_mult;
-    uint2* sm = reinterpret_cast<uint2*>(smem + OFF_M);
     uint32_t tcount = 0;
     bool ok = true;
-    // second-slot update of the previous tile's column, deferred so that the
-    // returning atomic's latency overlaps the next tile
+    // the second slot's update of the previous segment's row, deferred so that the
+    // returning atomic's latency overlaps the next segment
     unsigned long long* pend_ptr = nullptr;
     unsigned long long pend_old = 0ull, pend_x1 = 0ull;
-    // the same for the row's second slot, deferred to the end of the next segment
-    unsigned long long* rpend_ptr = nullptr;
-    unsigned long long rpend_old = 0ull, rpend_k1 = 0ull;
     Cursor cur{-1, 0, 0};
     Segment g;
     while (next_segment(P, cur, g)) {
@@ -343,76 +330,52 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
       int C1 = 0, C2 = 0;
       for (int ct = g.ct0; ct < g.ct1; ++ct, ++tcount) {
         const uint32_t acc = tcount & 1u, aph = (tcount >> 1) & 1u;
-        // on a timeout keep going (results are flagged invalid): every epilogue warp
-        // must pass the same named-barrier sequence
-        {  // every lane tests the barrier (no broadcast), one vote for the outcome
+        {  // every lane tests the barrier (no broadcast), one vote for the outcome; on a
+           // timeout keep going (the results are flagged invalid)
           const bool w = mbar_wait(&t_full[acc], aph, abort_flag, P.err, ERR_TIMEOUT_EPILOGUE, WAIT_LIMIT_NS);
           if (!__all_sync(0xffffffffu, w)) ok = false;
         }
         tc_fence_after();
-        const uint32_t par = tcount & 1u;
-        // the global second of the column this lane merges at the end of the tile,
-        // read from L2 now (it only grows, so any earlier value is a lower bound):
-        // a tile best below it changes neither slot and needs no atomics
-        // this tile's quadrant merge is done by two of the quarter's four warps (which two
-        // alternates by tile), 32 columns each
-        const bool merger = (q & 1) == static_cast<int>(tcount & 1u);
-        const int mcol = ct * BN + qt * 64 + (q >> 1) * 32 + lane;
-        unsigned long long csec = ~0ull;
-        if (!DUMP && merger && mcol < fp.n_b)
-          csec = __ldcg(P.colkeys + 2 * static_cast<int64_t>(fp.col_base + mcol) + 1);
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + qt * 64;
         float t1 = 0.f, t2 = 0.f;  // the row's top-2 over this tile (8-bit column index)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {  // 16-column sub-chunks of this warp's 64 columns
-          uint32_t v[16];
-          tmem_ld_32x32b_x16(taddr + c * 16, v);
+        {
+          uint32_t v[64];
+          tmem_ld_32x32b_x64(taddr, v);
           tmem_wait_ld();
           if constexpr (DUMP) {
             const int row = g.rt * BM + static_cast<int>(rl);
             if (row < fp.n_a) {
 #pragma unroll
-              for (int k = 0; k < 16; ++k) {
-                const int col = ct * BN + qt * 64 + c * 16 + k;
-                if (col < fp.n_b)
-                  P.dump[static_cast<int64_t>(row) * P.dump_ld + col] =
-                      static_cast<int32_t>(v[k] & 0x7FFFFFu);  // bits of 2^23 + s
+              for (int k = 0; k < 64; ++k) {
+                const int col = ct * BN + qt * 64 + k;
+                if (col < fp.n_b && ((row + col) & 1) == fp.transposed) {
+                  const int64_t at = fp.transposed ? static_cast<int64_t>(col) * P.dump_ld + row
+                                                   : static_cast<int64_t>(row) * P.dump_ld + col;
+                  P.dump[at] = static_cast<int32_t>(v[k] & 0x7FFFFFu);  // bits of 2^23 + s
+                }
               }
             }
           } else {
-            // row: keys (sub-chunk index 15 - k), reduced by a tree
-            float a1, a2;
-            {
-              float rk[16];
 #pragma unroll
-              for (int k = 0; k < 16; ++k) rk[k] = __uint_as_float(mad_lo(v[k], key_mult, 15u - k));
+            for (int c = 0; c < 2; ++c) {  // two 32-column halves, keys with a 5-bit index
+              float rk[32];
+#pragma unroll
+              for (int k = 0; k < 32; ++k) rk[k] = __uint_as_float(mad_lo(v[32 * c + k], key_mult, 31u - k));
+              float a1, a2;
               tree_top2(rk, a1, a2);
+              // half index (31 - k) -> tile-local 255 - (64 qt + 32 c + k)
+              const uint32_t chb = static_cast<uint32_t>(7 - 2 * qt - c) << 5;
+              merge2(t1, t2, __uint_as_float(__float_as_uint(a1) | chb), __uint_as_float(__float_as_uint(a2) | chb));
             }
-            // columns: the warp's best key per column is a warp-wide max; the second is
-            // the max of (key - best), which wraps the best lane to 0 and keeps the
-            // order of the others.  Lane 0 stores the 16 columns' (best, second - best)
-            // (mod 2^32); the quadrant merge adds the best back.
-            uint4* sm4 = reinterpret_cast<uint4*>(sm + (par * 4 + q) * BN + qt * 64 + c * 16);
-#pragma unroll
-            for (int k = 0; k < 16; k += 2) {
-              const uint32_t x0 = mad_lo(v[k], key_mult, col_low), x1 = mad_lo(v[k + 1], key_mult, col_low);
-              const uint32_t m0 = __reduce_max_sync(0xffffffffu, x0), m1 = __reduce_max_sync(0xffffffffu, x1);
-              const uint32_t s0 = __reduce_max_sync(0xffffffffu, x0 - m0);
-              const uint32_t s1 = __reduce_max_sync(0xffffffffu, x1 - m1);
-              if (lane == 0) sm4[k >> 1] = make_uint4(m0, s0, m1, s1);
-            }
-            // sub-chunk index (15 - k) -> tile-local 255 - (64 qt + 16 c + k)
-            const uint32_t chb = static_cast<uint32_t>(15 - 4 * qt - c) << 4;
-            merge2(t1, t2, __uint_as_float(__float_as_uint(a1) | chb), __uint_as_float(__float_as_uint(a2) | chb));
           }
         }
         // hand the buffer back to the MMA: every thread once its own loads are done
         tc_fence_before();
         mbar_arrive(&t_empty[acc]);
         if constexpr (!DUMP) {
-          // row: fold the tile's top-2 into the segment's.  Tiles come in column
-          // order, so a tile key displaces a held one only with a strictly larger
-          // score (k > (R | 255)); on equal scores the earlier, lower column stays.
+          // fold the tile's top-2 into the segment's.  Tiles come in column order, so a
+          // tile key displaces a held one only with a strictly larger score
+          // (k > (R | 255)); on equal scores the earlier, lower column stays.
           const uint32_t k1t = __float_as_uint(t1), k2t = __float_as_uint(t2);
           if (k1t > (R2 | 255u)) {
             if (k1t > (R1 | 255u)) {
@@ -426,52 +389,22 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
               C2 = ct;
             }
           }
-          // columns: merge the four row quadrants once all four have written
-          named_bar_sync(1 + qt, 128);  // the four quadrant warps of this quarter
-          if (pend_ptr) {
-            const unsigned long long lo = pend_old < pend_x1 ? pend_old : pend_x1;
-            if (lo) atomicMax(pend_ptr, lo);
-            pend_ptr = nullptr;
-          }
-          if (merger) {
-            const int col = qt * 64 + (q >> 1) * 32 + lane;
-            uint2 x = sm[(par * 4 + 0) * BN + col];
-            float m1 = __uint_as_float(x.x), m2 = __uint_as_float(x.y + x.x);
-#pragma unroll
-            for (int qq = 1; qq < 4; ++qq) {
-              x = sm[(par * 4 + qq) * BN + col];
-              merge2(m1, m2, __uint_as_float(x.x), __uint_as_float(x.y + x.x));
-            }
-            const int j = ct * BN + col;
-            if (j < fp.n_b) {
-              const uint32_t rbase = static_cast<uint32_t>(g.rt * BM);
-              const unsigned long long x1 = key64(__float_as_uint(m1), rbase);
-              const unsigned long long x2 = key64(__float_as_uint(m2), rbase);
-              if (x1 > csec) {
-                unsigned long long* ck = P.colkeys + 2 * static_cast<int64_t>(fp.col_base + j);
-                pend_old = atomicMax(ck, x1);
-                pend_x1 = x1;
-                pend_ptr = ck + 1;
-                if (x2) atomicMax(ck + 1, x2);
-              }
-            }
-          }
         }
       }
       if constexpr (!DUMP) {
-        if (rpend_ptr) {
-          const unsigned long long lo = rpend_old < rpend_k1 ? rpend_old : rpend_k1;
-          if (lo) atomicMax(rpend_ptr, lo);
-          rpend_ptr = nullptr;
+        if (pend_ptr) {
+          const unsigned long long lo = pend_old < pend_x1 ? pend_old : pend_x1;
+          if (lo) atomicMax(pend_ptr, lo);
+          pend_ptr = nullptr;
         }
         const int i = g.rt * BM + static_cast<int>(rl);
         const unsigned long long K1 = key64(R1, static_cast<uint32_t>(C1 * BN));
         const unsigned long long K2 = key64(R2, static_cast<uint32_t>(C2 * BN));
         if (ok && i < fp.n_a && K1) {
-          unsigned long long* rk = P.rowkeys + 2 * static_cast<int64_t>(fp.row_base + i);
-          rpend_old = atomicMax(rk, K1);
-          rpend_k1 = K1;
-          rpend_ptr = rk + 1;
+          unsigned long long* rk = fp.keys + 2 * static_cast<int64_t>(i);
+          pend_old = atomicMax(rk, K1);
+          pend_x1 = K1;
+          pend_ptr = rk + 1;
           if (K2) atomicMax(rk + 1, K2);
         }
       }
@@ -479,10 +412,6 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     if (pend_ptr) {
       const unsigned long long lo = pend_old < pend_x1 ? pend_old : pend_x1;
       if (lo) atomicMax(pend_ptr, lo);
-    }
-    if (rpend_ptr) {
-      const unsigned long long lo = rpend_old < rpend_k1 ? rpend_old : rpend_k1;
-      if (lo) atomicMax(rpend_ptr, lo);
     }
   }
 
@@ -500,15 +429,14 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
 int fused_smem_bytes() { return SMEM_TOTAL; }
 
 int launch_fused(const FusedParams& p, const void* tmap, bool dump, void* stream) {
-  static bool configured[2] = {false, false};
-  const int idx = dump ? 1 : 0;
-  cudaError_t e;
-  if (!configured[idx]) {
-    e = dump ? cudaFuncSetAttribute(fused_top2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL)
-             : cudaFuncSetAttribute(fused_top2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
-    if (e != cudaSuccess) return static_cast<int>(e);
-    configured[idx] = true;
-  }
+  // the opt-in to more than 48 KB of dynamic shared memory is an attribute of the
+  // function on the current device: set it on every launch (cheap), so that every
+  // device the caller makes current gets it
+  cudaError_t e = dump ? cudaFuncSetAttribute(fused_top2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              SMEM_TOTAL)
+                       : cudaFuncSetAttribute(fused_top2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              SMEM_TOTAL);
+  if (e != cudaSuccess) return static_cast<int>(e);
   CUtensorMap map;
   memcpy(&map, tmap, sizeof(map));
   cudaLaunchConfig_t cfg = {};

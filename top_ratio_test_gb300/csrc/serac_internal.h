@@ -1,19 +1,25 @@
 // Internal layout shared by the host scheduler (api.cu) and the kernels.
 //
-// Tiling: a pair's score matrix is cut into tiles of BM = 128 rows of A (one
-// tcgen05 accumulator: TMEM lane = row) by BN = 256 rows of B (TMEM columns).
-// Every image is staged once as bf16, zero-padded to a multiple of 256 rows, into
-// one buffer that a single TMA tensor map covers; the zero rows score 0 and the
-// zero floor drops them, so ragged tails need no masking.
+// Both directions of a pair are row problems.  The column top-2 of the pair (A, B) is
+// the row top-2 of (B, A), so every pair is matched as two problems of the same kind:
+// rows of A against the columns B, and rows of B against the columns A.  The fused
+// kernel only ever keeps row top-2s.
+//
+// Tiling: a problem's score matrix is cut into tiles of BM = 128 rows (one tcgen05
+// accumulator: TMEM lane = row) by BN = 256 columns (TMEM columns).  Every image is
+// staged once as bf16, zero-padded to a multiple of 256 rows, into one buffer that a
+// single TMA tensor map covers; the zero rows score 0 and the zero floor drops them,
+// so ragged tails need no masking.
 //
 // Work: in a launch chunk, every CTA of the persistent fused kernel takes one piece
-// of every pair (piece k of pair p goes to CTA (offset_p + k) mod grid; a pair's T
-// tiles are dealt T / grid per piece, one more for the first T mod grid pieces, and
-// a pair with fewer tiles than CTAs has one-tile pieces).  A piece is a run of the pair's tiles in
-// row-major order, processed as segments: one A tile resident in shared memory
-// against a run of B tiles of one row tile, with one running row top-2.  All CTAs thus
-// work through the pairs in the same order, so the operands of the pairs in flight
-// stay in L2, and every CTA gets the same number of tiles within one per pair.
+// of every problem (piece k of problem p goes to CTA (offset_p + k) mod grid; a
+// problem's T tiles are dealt T / grid per piece, one more for the first T mod grid
+// pieces, and a problem with fewer tiles than CTAs has one-tile pieces).  A piece is a
+// run of the problem's tiles in row-major order, processed as segments: one row tile
+// resident in shared memory against a run of column tiles, with one running top-2 per
+// row.  All CTAs thus work through the problems in the same order (a pair's two
+// problems one after the other), so the operands in flight stay in L2, and every CTA
+// gets the same number of tiles within one per problem.
 #pragma once
 #include <stdint.h>
 
@@ -35,31 +41,33 @@ constexpr int ERR_TIMEOUT_MMA = 2;
 constexpr int ERR_TIMEOUT_EPILOGUE = 4;
 constexpr int ERR_TIMEOUT_LOOKBACK = 8;
 
+// One row problem: rows of one staged image against the rows (columns of the score
+// matrix) of another.
 struct FusedPair {
-  int32_t a_row0;      // first staged row of image A
-  int32_t b_row0;      // first staged row of image B
-  int32_t n_a, n_b;
-  int32_t npieces;     // pieces the pair's tiles are cut into (<= grid)
+  int32_t a_row0;      // first staged row of the row-side image
+  int32_t b_row0;      // first staged row of the column-side image
+  int32_t n_a, n_b;    // rows, columns
+  int32_t npieces;     // pieces the problem's tiles are cut into (<= grid)
   int32_t offset;      // piece k goes to CTA (offset + k) mod grid
-  int32_t row_base;    // first row-key entry of this pair
-  int32_t col_base;    // first column-key entry of this pair
+  int32_t transposed;  // score dump only: rows are the pair's B (write S[col][row])
+  int32_t pad_;
+  unsigned long long* keys;  // [n_a][2] row keys of this problem (rowkeys or colkeys of the pair)
 };
 
 // Final top-2 of a row or column as two 64-bit keys (best, second):
 // key = score << 32 | (0xFFFFFFFF - index), 0 = empty.  A plain unsigned max orders
 // by score, then lower index.  Kernels merge into them with atomicMax.
+constexpr int MAX_PROBLEMS = 2 * MAX_PAIRS;
 struct FusedParams {
-  int32_t n_pairs;
+  int32_t n_pairs;                   // row problems in the launch
   int32_t grid;
   int32_t dump_ld;                   // score-dump row stride (dump mode only)
-  unsigned long long* rowkeys;       // [rows of the chunk][2]
-  unsigned long long* colkeys;       // [columns of the chunk][2]
   int32_t* err;                      // error bits
   int32_t* dump;                     // score dump (dump mode only)
   uint32_t key_mult;                 // 256, read as a kernel parameter (see the epilogue)
   int32_t no_copies;                 // test hook: the producer issues no copies (bounded waits run out)
   int32_t early_dependents;          // let the match launch start beside this kernel's CTAs
-  FusedPair pairs[MAX_PAIRS];
+  FusedPair pairs[MAX_PROBLEMS];
 };
 
 struct StageImage {
@@ -103,8 +111,6 @@ struct FinishParams {
   const unsigned long long* rowkeys;
   const unsigned long long* colkeys;
   int32_t* tickets;               // [pair]: next block index of the pair (zeroed)
-  int32_t index_order;            // 1: block order = block index (the whole grid fits the GPU)
-  int32_t pad_;
   unsigned long long* status;     // [block]: look-back word (zeroed)
   uint4* zero;                    // the other chunk's key region, cleared here
   int64_t zero_n;                 // 16-byte words
