@@ -39,6 +39,36 @@ def test_noalloc_matches_match_pair_twice(serac):
         assert len(ref[0]) > 0
 
 
+def test_noalloc_allocates_nothing(serac):
+    """After the first call in this context (which looks up the scratch's address),
+    further calls through the raw C ABI change neither the device's free memory nor
+    the caching allocator's reservations: no cudaMalloc, no cudaFree, nothing pooled."""
+    import ctypes
+    p = S.single_pair_2000(0)
+    a = torch.from_numpy(p.a).cuda()
+    b = torch.from_numpy(p.b).cuda()
+    params = serac.default_params()
+    o, c = serac._make_out(2000, 2000, a.device, None, True)
+    ref = _outputs(serac.match_pair(a, b, top2=True))
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def call():
+        return serac.lib().match_pair_noalloc(a.data_ptr(), 2000, b.data_ptr(), 2000, ctypes.byref(params),
+                                              ctypes.byref(c), stream)
+
+    assert call() == serac.OK
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    reserved0 = torch.cuda.memory_reserved()
+    for _ in range(3):
+        assert call() == serac.OK
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_reserved() == reserved0
+    for x, y in zip(_outputs(o), ref):
+        np.testing.assert_array_equal(x, y)
+
+
 def test_noalloc_rejects_oversized_pairs(serac):
     n = 32768
     assert serac.pair_workspace_size(16384, 16384) <= serac.NOALLOC_SCRATCH_BYTES
