@@ -28,7 +28,9 @@ match_batch over the whole workload per step, with the same keys.
 pages publish no runnable reference for this path; the oracle is the baseline arm).
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload (weak
-scaling, no data-path collective); time is the max over ranks.
+scaling, no data-path collective); time is the max over ranks.  --shard (batch
+workloads) splits the workload's pairs over the ranks by cost instead (strong
+scaling); rank 0 then gathers every pair's match list after the timed steps.
 """
 from __future__ import annotations
 
@@ -50,10 +52,13 @@ N_A = N_B = 8192
 OPS_PER_PAIR = 2 * N_A * N_B * 128
 WORKLOAD = "single pair 8192x8192 SIFT-shaped u8 descriptors, 25% planted at sigma 0.08, seed 0"
 WORKLOAD_2000 = "single pair 2000x2000 SIFT-shaped u8 descriptors, 30% planted at sigma 0.05, seed 0"
-# DRAM bytes (read + write) of one fused_top2_kernel launch on the 8192 x 8192 pair, from
-# the ncu capture summarised in profiles/fused_top2_pair_8192x8192_full.md; None whenever
-# the kernel has changed since that capture
-FUSED_TRAFFIC_8192 = 4492288
+# DRAM bytes (read + write) of one fused_top2_kernel launch on the 8192 x 8192 pair, as
+# measured by the latest ncu capture of the kernel as it stands (dram__bytes_read.sum +
+# dram__bytes_write.sum); None whenever the kernel has changed since that capture
+FUSED_TRAFFIC_8192 = None
+# the arithmetic of the path: u8 inputs, exact integer scores formed on the tensor
+# cores from bf16 operands with f32 accumulation (every partial sum < 2^24)
+DTYPE = "u8 exact (bf16 operands, f32 accumulate)"
 
 
 def _peaks():
@@ -360,7 +365,7 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE, "data": "synthetic",
         "config": {"workload": (f"single pair {n_a}x{n_b} SIFT-shaped u8 descriptors, 25% planted at sigma 0.08, "
                                 f"seed 0" if args.n else WORKLOAD if args.workload == "pair8192" else WORKLOAD_2000),
                    "n_a": n_a, "n_b": n_b,
@@ -426,9 +431,18 @@ def run_batch(args):
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
-    desc, imgs_np, pairs_idx = _batch_workload(args.workload)
+    desc, imgs_np, all_idx = _batch_workload(args.workload)
+    # replicas: every rank matches the whole workload (weak scaling); --shard: the pairs
+    # are split over the ranks by cost and every rank matches its own share (strong)
+    shard = args.shard and world > 1
+    mine = list(range(len(all_idx)))
+    if shard:
+        sizes = [(imgs_np[i].shape[0], imgs_np[j].shape[0]) for i, j in all_idx]
+        mine = serac.shard_pairs(sizes, world)[rank]
+    pairs_idx = [all_idx[k] for k in mine]
     imgs = [torch.from_numpy(x).to(dev) for x in imgs_np]
     pairs = [(imgs[i], imgs[j]) for i, j in pairs_idx]
+    ops_all = sum(2 * imgs_np[i].shape[0] * imgs_np[j].shape[0] * 128 for i, j in all_idx)
     ops = sum(2 * imgs_np[i].shape[0] * imgs_np[j].shape[0] * 128 for i, j in pairs_idx)
     params = serac.default_params()
     stream = torch.cuda.Stream(device=dev)
@@ -464,16 +478,21 @@ def run_batch(args):
     clk = clocks.stop()
     total_ms = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in evs), dev)
     n_pairs = len(pairs)
-    value = world * n_pairs * args.steps / (total_ms * 1e-3)
-    tops = world * ops * args.steps / (total_ms * 1e-3) / 1e12
+    # pairs and ops of the whole job: every rank's replica, or the one sharded workload
+    job_pairs = len(all_idx) if shard else world * n_pairs
+    job_ops = ops_all if shard else world * ops
+    value = job_pairs * args.steps / (total_ms * 1e-3)
+    tops = job_ops * args.steps / (total_ms * 1e-3) / 1e12
     peak_tflops, _, peak_kind = _peaks()
     line = {"metric": "image pairs/sec (batch), int8-equivalent TOPS", "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": {"workload": desc, "pairs": n_pairs,
+            "higher_is_better": True, "scaling": "strong" if shard else "weak", "vs_baseline": None,
+            "dtype": DTYPE,
+            "data": "synthetic", "config": {"workload": desc, "pairs": len(all_idx),
                                              "l2": "flushed before every step (256 MiB write)",
                                              "graph": "one CUDA graph per step (match_batch), replayed",
-                                             "parallelism": f"replicas x{world}"},
+                                             "parallelism": (f"pairs sharded by cost over {world} GPUs" if shard
+                                                             else f"replicas x{world}")},
             "int8_equiv_tops": tops,
             "roofline": {"bound": "tensor", "achieved": tops, "peak": peak_tflops, "unit": "TFLOP/s",
                          "frac": tops / world / peak_tflops, "traffic": None,
@@ -503,7 +522,12 @@ def run_batch(args):
     stream.synchronize()
     e2e_ms = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in e2e_evs), dev)
     same = all(torch.equal(o.result(), h.result()) for o, h in zip(outs, e2e_outs))
-    line["e2e"] = {"value": world * n_pairs * e2e_steps / (e2e_ms * 1e-3), "unit": UNIT,
+    if shard:
+        # collect every pair's match list on rank 0 (host side, after the timed work)
+        got = serac.gather_matches(mine, outs, len(all_idx))
+        if rank == 0:
+            line["gathered_pairs"] = sum(1 for m in got if m is not None)
+    line["e2e"] = {"value": job_pairs * e2e_steps / (e2e_ms * 1e-3), "unit": UNIT,
                    "h2d_bytes_per_step": sum(x.shape[0] * 128 for x in imgs_np),
                    "d2h_bytes_per_step": sum(4 + 8 * int(h.count.item()) for h in e2e_outs),
                    "steps": e2e_steps, "equals_device_resident_result": bool(same),
@@ -546,6 +570,9 @@ def main():
     ap.add_argument("--workload", choices=["pair8192", "pair2000", "ring12", "ragged256", "survey100"],
                     default="pair8192", help="pair8192 is the headline; the others are batch lines "
                     "for the tables (match_batch over the whole workload per step)")
+    ap.add_argument("--shard", action="store_true",
+                    help="batch workloads on several GPUs: split the pairs over the ranks by cost "
+                    "(strong scaling) instead of running a replica per rank")
     ap.add_argument("--n", type=int, default=0,
                     help="a single n x n pair (same recipe as the 8192 x 8192 one) instead of the workload")
     args = ap.parse_args()

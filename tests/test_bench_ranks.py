@@ -106,3 +106,48 @@ def test_shard_pairs_edge_cases():
     assert serac.shard_pairs([], 3) == [[], [], []]
     assert serac.shard_pairs([(5, 5)], 1) == [[0]]
     assert serac.shard_pairs([(10, 10), (1, 1), (10, 10)], 2) == [[0, 1], [2]]
+
+
+class _FakeOut:
+    """Stands in for a MatchOutput on CPU: result() gives the pair's match list."""
+
+    def __init__(self, k):
+        import torch
+        self.m = torch.tensor([[k, 1000 + k], [k + 1, 2000 + k]], dtype=torch.int32)[: 1 + k % 2]
+
+    def result(self):
+        return self.m
+
+
+def _gather_worker(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import sift_synth
+    import top_ratio_test_gb300 as serac
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    sizes = [tuple(int(v) for v in x) for x in sift_synth.ragged_sizes(0)]
+    mine = serac.shard_pairs(sizes, world)[rank]
+    outs = [_FakeOut(k) for k in mine]
+    got = serac.gather_matches(mine, outs, len(sizes))
+    q.put((rank, None if got is None else [m.tolist() for m in got]))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_gather_matches_gloo():
+    """The host-side collection of a sharded batch over two gloo ranks: rank 0 gets
+    every pair's match list, in pair order, each from the rank that matched it."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_gather_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=180) for _ in range(2))
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert res[1] is None
+    assert res[0] == [_FakeOut(k).m.tolist() for k in range(256)]

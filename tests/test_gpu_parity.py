@@ -31,14 +31,15 @@ def _run_pair(serac, a, b, params=None, capacity=None):
 
 
 def _oracle_params(oracle_mod, p):
-    return oracle_mod.Params(p.ratio_num_sq, p.ratio_den_sq, p.norm_sq, p.min_score, p.mutual, p.col_ratio)
+    return oracle_mod.Params(p.ratio_num_sq, p.ratio_den_sq, p.norm_sq, p.min_score, p.mutual, p.col_ratio,
+                             p.max_features)
 
 
 def _assert_pair(serac, oracle_mod, a, b, params=None):
     p = params if params is not None else serac.default_params()
     out = _run_pair(serac, a, b, p)
     ref = oracle_mod.match(a, b, _oracle_params(oracle_mod, p))
-    na, nb = a.shape[0], b.shape[0]
+    na, nb = ref.row_top2.shape[0], ref.col_top2.shape[0]
     np.testing.assert_array_equal(out.row_top2.cpu().numpy()[:na], ref.row_top2)
     np.testing.assert_array_equal(out.col_top2.cpu().numpy()[:nb], ref.col_top2)
     np.testing.assert_array_equal(out.result().numpy(), ref.matches)
@@ -352,36 +353,107 @@ def test_batch_concurrent_host_threads(serac, oracle_mod):
             np.testing.assert_array_equal(outs[k].result().numpy(), refs[(i, j)], err_msg=f"{name} pair {k}")
 
 
+def test_exact_beside_a_saturating_stream(serac, oracle_mod):
+    """Calls that run while another stream keeps the SMs busy (a chain of large bf16
+    GEMMs) still return exact results: the match kernel's blocks only wait on blocks
+    that already run (tickets), whatever else occupies the GPU."""
+    p = S.single_pair_2000(0)
+    ref = oracle_mod.match(p.a, p.b)
+    a, b = _dev(p.a), _dev(p.b)
+    x = torch.randn(8192, 8192, device="cuda", dtype=torch.bfloat16)
+    other = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(other):
+        for _ in range(40):
+            x = torch.nn.functional.normalize(x @ x, dim=1).to(torch.bfloat16)
+    outs = [serac.match_pair(a, b, top2=True) for _ in range(25)]
+    torch.cuda.synchronize()
+    for o in outs:
+        np.testing.assert_array_equal(o.result().numpy(), ref.matches)
+        np.testing.assert_array_equal(o.row_top2.cpu().numpy(), ref.row_top2)
+        np.testing.assert_array_equal(o.col_top2.cpu().numpy(), ref.col_top2)
+
+
 def test_batch_ragged_256(serac, oracle_mod):
-    """256 ragged pairs (1,000..16,384 features): 12 pairs checked in full, every
-    pair checked on 48 sampled rows (top-2 and decision) and 48 sampled columns."""
+    """256 ragged pairs (1,000..16,384 features per image) through one match_batch:
+    every pair compared in full with the oracle -- row top-2, column top-2 and the
+    match list with its order."""
     sizes = S.ragged_sizes(0)
     pairs = [S.ragged_pair(0, k, sizes) for k in range(256)]
     dev = [(_dev(p.a), _dev(p.b)) for p in pairs]
     outs = serac.match_batch(dev, top2=True)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(5)
-    full = set(rng.choice(256, 12, replace=False).tolist())
-    par = oracle_mod.Params()
     for k, p in enumerate(pairs):
+        ref = oracle_mod.match(p.a, p.b)
         o = outs[k]
-        rows_t = o.row_top2.cpu().numpy()
-        cols_t = o.col_top2.cpu().numpy()
-        m = o.result().numpy()
-        if k in full:
-            ref = oracle_mod.match(p.a, p.b)
-            np.testing.assert_array_equal(rows_t, ref.row_top2)
-            np.testing.assert_array_equal(cols_t, ref.col_top2)
-            np.testing.assert_array_equal(m, ref.matches)
-            continue
-        ri = rng.choice(p.a.shape[0], 48, replace=False).astype(np.int32)
-        cj = rng.choice(p.b.shape[0], 48, replace=False).astype(np.int32)
-        j, rt, _ = oracle_mod.accept_rows(p.a, p.b, ri, par)
-        np.testing.assert_array_equal(rows_t[ri], rt)
-        np.testing.assert_array_equal(cols_t[cj], oracle_mod.col_top2(p.a, p.b, cj))
-        kept = dict(zip(m[:, 0].tolist(), m[:, 1].tolist()))
-        assert [kept.get(int(i), -1) for i in ri] == j.tolist()
-        assert np.all(np.diff(m[:, 0]) > 0)
+        np.testing.assert_array_equal(o.row_top2.cpu().numpy(), ref.row_top2, err_msg=f"pair {k} rows")
+        np.testing.assert_array_equal(o.col_top2.cpu().numpy(), ref.col_top2, err_msg=f"pair {k} columns")
+        np.testing.assert_array_equal(o.result().numpy(), ref.matches, err_msg=f"pair {k} matches")
+
+
+@pytest.mark.parametrize("ratio,angle", [(0.7, 0.6), (0.9, 0.8), (0.75, 0.5), (1.0, 0.9)])
+def test_other_ratios_and_angles(serac, oracle_mod, ratio, angle):
+    """Parameters other than 0.8 / 0.7 rad, derived by serac_default_params (and by the
+    oracle separately), on the 2,000 x 2,000 pair and on a pair of ties."""
+    p = serac.default_params(ratio, angle)
+    q = oracle_mod.default_params(ratio, angle)
+    assert (p.ratio_num_sq, p.ratio_den_sq, p.min_score) == (q.ratio_num_sq, q.ratio_den_sq, q.min_score)
+    pr = S.single_pair_2000(0)
+    out, ref = _assert_pair(serac, oracle_mod, pr.a, pr.b, p)
+    assert len(ref.matches) > 0
+    rng = np.random.default_rng(12)
+    vals = np.array([0, 1, 2, 255], np.uint8)
+    a = vals[rng.integers(0, 4, size=(400, 128))]
+    b = vals[rng.integers(0, 4, size=(300, 128))]
+    a[rng.random(a.shape) < 0.6] = 0
+    b[rng.random(b.shape) < 0.6] = 0
+    b[100:140] = b[1]
+    p.norm_sq = 3_000_000
+    _assert_pair(serac, oracle_mod, a, b, p)
+
+
+@pytest.mark.parametrize("cap", [1, 700, 1999, 2000, 5000])
+def test_feature_cap(serac, oracle_mod, cap):
+    """max_features = K matches only the first K descriptors of each image (the match
+    cap of the SERAC page, section 'Memory'): equal to the oracle under the same cap and
+    to a plain match of the truncated images."""
+    pr = S.make_pair(3, 67, 0, 2000, 3000, 0.3, 0.05)
+    p = serac.default_params(max_features=cap)
+    out, ref = _assert_pair(serac, oracle_mod, pr.a, pr.b, p)
+    k_a, k_b = min(cap, 2000), min(cap, 3000)
+    assert out.row_top2.shape[0] == max(k_a, 1) and out.col_top2.shape[0] == max(k_b, 1)
+    plain = oracle_mod.match(pr.a[:k_a], pr.b[:k_b])
+    np.testing.assert_array_equal(out.result().numpy(), plain.matches)
+    # the same cap through match_batch, next to an uncapped-size pair
+    outs = serac.match_batch([(_dev(pr.a), _dev(pr.b)), (_dev(pr.b[:900]), _dev(pr.a[:500]))], p, top2=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(outs[0].result().numpy(), ref.matches)
+    ref2 = oracle_mod.match(pr.b[:900], pr.a[:500], oracle_mod.Params(max_features=cap))
+    np.testing.assert_array_equal(outs[1].result().numpy(), ref2.matches)
+    np.testing.assert_array_equal(outs[1].row_top2.cpu().numpy()[:min(cap, 900)], ref2.row_top2)
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_sharded_batch_equals_unsharded(serac, oracle_mod, world):
+    """A batch split over `world` GPUs by shard_pairs, each shard run by its own
+    match_batch (here one after another on one GPU), gives every pair exactly the
+    match list (and top-2 tables) of the unsharded match_batch."""
+    sizes = S.ragged_sizes(0)[:40] // 4
+    pairs_np = [S.make_pair(9, 68, k, int(sizes[k, 0]), int(sizes[k, 1]), 0.15, 0.05) for k in range(40)]
+    dev = [(_dev(p.a), _dev(p.b)) for p in pairs_np]
+    whole = serac.match_batch(dev, top2=True)
+    torch.cuda.synchronize()
+    seen = []
+    for rank in range(world):
+        mine, outs = serac.match_batch_shard(dev, rank, world, top2=True)
+        torch.cuda.synchronize()
+        seen += mine
+        for k, o in zip(mine, outs):
+            assert torch.equal(o.result(), whole[k].result()), (rank, k)
+            assert torch.equal(o.row_top2, whole[k].row_top2) and torch.equal(o.col_top2, whole[k].col_top2)
+    assert sorted(seen) == list(range(40))
+    for k in (0, 17, 39):
+        np.testing.assert_array_equal(whole[k].result().numpy(), oracle_mod.match(pairs_np[k].a, pairs_np[k].b).matches)
 
 
 def test_batch_survey_spot_50(serac, oracle_mod):
