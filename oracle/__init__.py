@@ -91,6 +91,7 @@ def _load():
         lib.oracle_col_top2.argtypes = [P, i32, P, i32, P, i32, P]
         lib.oracle_match.argtypes = [P, i32, P, i32, ctypes.POINTER(_Params), P, P, P, i32, P]
         lib.oracle_accept_rows.argtypes = [P, i32, P, i32, ctypes.POINTER(_Params), P, i32, P, P, P]
+        lib.oracle_row_topk.argtypes = [P, i32, P, i32, i32, P, i32, P, P]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         _lib = lib
@@ -145,6 +146,19 @@ def col_top2(a: np.ndarray, b: np.ndarray, cols=None) -> np.ndarray:
     rc = _load().oracle_col_top2(_ptr(a), a.shape[0], _ptr(b), b.shape[0], _ptr(c), n, _ptr(out))
     assert rc == 0
     return out
+
+
+def row_topk(a: np.ndarray, b: np.ndarray, k: int, rows=None):
+    """Row top-k: (scores, index), each (n, k) int32, the first k candidates of every
+    row (score descending, index ascending, zero scores excluded), padded (0, -1)."""
+    a, b = _u8(a), _u8(b)
+    r = None if rows is None else np.ascontiguousarray(rows, np.int32)
+    n = a.shape[0] if r is None else r.shape[0]
+    sc = np.zeros((n, max(k, 1)), np.int32)
+    ix = np.zeros((n, max(k, 1)), np.int32)
+    rc = _load().oracle_row_topk(_ptr(a), a.shape[0], _ptr(b), b.shape[0], int(k), _ptr(r), n, _ptr(sc), _ptr(ix))
+    assert rc == 0, rc
+    return sc, ix
 
 
 @dataclass

@@ -34,6 +34,12 @@
  *   column direction (ColMatch) feeds the cross check.  Matches are listed by
  *   ascending i.
  *
+ *   Row top-k (guided matching): the first k entries of the same candidate list of row
+ *   i, padded with (0, -1).  The pages keep k = 2 ("Real-Time Dense Stereo at 34 Hz on
+ *   a Jetson TX2 (MASDA, Part 3)", the CPU/GPU interface keeps two scored candidates
+ *   per pixel) and give the order and the zero floor for it ("SERAC", "Exactness");
+ *   for k > 2 the plainest reading keeps both: k = 2 is the row top-2 above.
+ *
  *   Feature cap (the match cap of the "SERAC" page, section "Memory": COLMAP advises
  *   lowering it when memory is short, and the features past it are clamped away).
  *   With max_features = K > 0 each image takes part with its first K descriptors
@@ -181,6 +187,35 @@ int oracle_col_top2(const uint8_t* A, int32_t nA, const uint8_t* B, int32_t nB,
     int32_t j = cols ? cols[c] : c;
     oracle_top2 t = col_top2(A, nA, B, j);
     put4(out + (size_t)c * 4, &t);
+  }
+  return 0;
+}
+
+/* Row top-k for the listed rows (all rows when rows == NULL): scores[r][k] and
+ * index[r][k], the first k candidates of the row in the order "score descending, index
+ * ascending" (zero scores are no candidates), padded with (0, -1). */
+int oracle_row_topk(const uint8_t* A, int32_t nA, const uint8_t* B, int32_t nB, int32_t k,
+                    const int32_t* rows, int32_t n_rows, int32_t* scores, int32_t* index) {
+  if (nA < 0 || nB < 0 || k < 1 || !scores || !index) return -1;
+  int32_t n = rows ? n_rows : nA;
+  for (int32_t r = 0; rows && r < n; ++r)
+    if (rows[r] < 0 || rows[r] >= nA) return -1;
+  #pragma omp parallel for schedule(dynamic, 16)
+  for (int32_t r = 0; r < n; ++r) {
+    int32_t i = rows ? rows[r] : r;
+    int32_t* ts = scores + (size_t)r * k;
+    int32_t* tj = index + (size_t)r * k;
+    for (int32_t q = 0; q < k; ++q) { ts[q] = 0; tj[q] = -1; }
+    for (int32_t j = 0; j < nB; ++j) {
+      int64_t s = dot128(A + (size_t)i * ORACLE_DIM, B + (size_t)j * ORACLE_DIM);
+      if (s <= 0) continue; /* zero floor */
+      int32_t pos = 0;      /* first slot the candidate comes before */
+      while (pos < k && !before(s, j, ts[pos], tj[pos])) ++pos;
+      if (pos == k) continue;
+      for (int32_t q = k - 1; q > pos; --q) { ts[q] = ts[q - 1]; tj[q] = tj[q - 1]; }
+      ts[pos] = (int32_t)s;
+      tj[pos] = j;
+    }
   }
   return 0;
 }

@@ -14,7 +14,10 @@ Each test names the mistakes it is there to catch:
   the same test;
 * the bound s <= N = 512^2 on generated descriptors (Cauchy-Schwarz after floor
   quantisation);
-* the derivation of the default parameters from 0.8 and 0.7 rad.
+* the derivation of the default parameters from 0.8 and 0.7 rad;
+* row top-k: a hand-worked k = 6 example (ties in column order, zero floor, padding),
+  a Python brute force on tiny inputs, k = 2 against the row top-2, and every k a
+  prefix of k + 1.
 """
 import json
 import math
@@ -254,3 +257,75 @@ def test_score_bound_on_generated_data(oracle_mod):
     assert s.max() <= 512 * 512
     na = (p.a.astype(np.int64) ** 2).sum(1)
     assert na.max() <= 512 * 512
+
+
+# ------------------------------------------------------------------ row top-k
+
+def test_row_topk_hand(oracle_mod):
+    g = _load("row_topk.json")
+    vec = {k: _vec(v) for k, v in g["vectors"].items()}
+    A = np.stack([vec[k] for k in g["A"]])
+    B = np.stack([vec[k] for k in g["B"]])
+    assert oracle_mod.scores(A, B).tolist() == g["scores"]
+    sc, ix = oracle_mod.row_topk(A, B, g["k"])
+    assert sc.tolist() == g["top_scores"]
+    assert ix.tolist() == g["top_index"]
+    for k in range(1, g["k"] + 1):   # every k is the first k columns of the k = 6 lists
+        sk, ik = oracle_mod.row_topk(A, B, k)
+        assert sk.tolist() == [r[:k] for r in g["top_scores"]]
+        assert ik.tolist() == [r[:k] for r in g["top_index"]]
+
+
+def _topk_brute(A, B, k):
+    """Python loops: every candidate of the row, sorted by (-s, j), first k, padded."""
+    out_s, out_j = [], []
+    for i in range(A.shape[0]):
+        cand = []
+        for j in range(B.shape[0]):
+            s = sum(int(x) * int(y) for x, y in zip(A[i], B[j]))
+            if s > 0:
+                cand.append((-s, j))
+        cand.sort()
+        cand = cand[:k] + [(0, -1)] * max(0, k - len(cand))
+        out_s.append([-c[0] if c[1] >= 0 else 0 for c in cand])
+        out_j.append([c[1] for c in cand])
+    return out_s, out_j
+
+
+@pytest.mark.parametrize("na,nb,k,seed", [(0, 5, 3, 0), (4, 0, 3, 1), (1, 1, 1, 2), (7, 9, 4, 3),
+                                          (12, 10, 8, 4), (5, 3, 7, 5), (9, 16, 2, 6)])
+def test_row_topk_brute_force(oracle_mod, na, nb, k, seed):
+    rng = np.random.default_rng([seed, 77])
+    # few distinct values so that ties are common, plus all-zero rows and columns
+    A = rng.integers(0, 3, (na, 128)).astype(np.uint8) * rng.integers(0, 2, (na, 1)).astype(np.uint8)
+    B = rng.integers(0, 3, (nb, 128)).astype(np.uint8)
+    if nb > 2:
+        B[1] = B[nb - 1]            # duplicated columns: equal scores, lower index first
+        B[0] = 0
+    bs, bj = _topk_brute(A, B, k)
+    sc, ix = oracle_mod.row_topk(A, B, k)
+    assert sc.tolist() == bs and ix.tolist() == bj
+
+
+def test_row_topk_k2_is_row_top2(oracle_mod):
+    p = S.single_pair_2000(0)
+    a, b = p.a[:300], p.b[:700]
+    b = np.concatenate([b, b[:50]])   # exact ties with lower columns
+    sc, ix = oracle_mod.row_topk(a, b, 2)
+    t2 = oracle_mod.row_top2(a, b)
+    assert np.array_equal(np.stack([sc[:, 0], ix[:, 0], sc[:, 1], ix[:, 1]], 1), t2)
+
+
+def test_row_topk_rows_and_arguments(oracle_mod):
+    p = S.single_pair_2000(0)
+    a, b = p.a[:64], p.b[:200]
+    sc, ix = oracle_mod.row_topk(a, b, 5)
+    rows = np.array([63, 0, 17, 17], np.int32)
+    s2, i2 = oracle_mod.row_topk(a, b, 5, rows=rows)
+    assert np.array_equal(s2, sc[rows]) and np.array_equal(i2, ix[rows])
+    lib = oracle_mod._load()
+    out = np.zeros((64, 1), np.int32)
+    P = oracle_mod._ptr
+    assert lib.oracle_row_topk(P(a), 64, P(b), 200, 0, None, 0, P(out), P(out)) == -1   # k < 1
+    bad = np.array([64], np.int32)
+    assert lib.oracle_row_topk(P(a), 64, P(b), 200, 1, P(bad), 1, P(out), P(out)) == -1  # row out of range
