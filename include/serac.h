@@ -144,6 +144,32 @@ int match_batch(const serac_pair* pairs, int32_t n_pairs, const serac_params* pa
 int serac_scores(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b, int32_t n_b,
                  int32_t* scores, void* workspace, size_t workspace_bytes, void* cuda_stream);
 
+/* Row top-k for guided matching (k = 1..SERAC_MAX_TOPK): for every row i of A, the k
+ * highest-scoring columns of B, in the order of the method's candidate list -- score
+ * descending, then lower column first, zero scores excluded ("SERAC" page,
+ * "Exactness"; the pages keep k = 2, "Real-Time Dense Stereo at 34 Hz on a Jetson TX2
+ * (MASDA, Part 3)" on the two scored candidates per pixel) -- padded with (0, -1).
+ * scores[i * k + q] and index[i * k + q] (int32, device or pinned host memory, 4-byte
+ * aligned) get entry q of row i; for k = 2 they equal the (s1, s2) and (j1, j2) of
+ * match_pair's row top-2.  No ratio test or cross check is applied: the list is the
+ * candidate set for a later geometric (guided) test.  `status` (int32, device or
+ * pinned host, may be NULL) receives SERAC_OK, or SERAC_ETIMEOUT when a bounded wait
+ * inside a kernel ran out (then scores and index are not valid), once the stream has
+ * run the call.  Workspace: device memory of at least serac_topk_workspace_size(n_a,
+ * n_b, k) bytes, 256-byte aligned, scratch for this call.  Argument errors:
+ * SERAC_EINVAL (k outside 1..SERAC_MAX_TOPK, sizes outside 0..SERAC_MAX_N, NULL or
+ * misaligned pointers), SERAC_EWORKSPACE, SERAC_ECUDA, SERAC_EUNSUPPORTED. */
+#define SERAC_MAX_TOPK 8
+
+/* Workspace bytes serac_topk_pair needs on the current device (the split of the work
+ * over the device's SMs sets it); 0 if the device cannot be queried or an argument is
+ * out of range.  Host only. */
+size_t serac_topk_workspace_size(int32_t n_a, int32_t n_b, int32_t k);
+
+int serac_topk_pair(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b, int32_t n_b, int32_t k,
+                    int32_t* scores, int32_t* index, int32_t* status, void* workspace, size_t workspace_bytes,
+                    void* cuda_stream);
+
 /* Profiling hook: when both events are non-NULL (cudaEvent_t), every following
  * match_pair / match_batch call made by the calling thread records `ev_begin` just
  * before its first fused GEMM + top-2 launch and `ev_end` just after it, on the

@@ -197,3 +197,22 @@ def test_timeout_hook_is_host_only(serac):
     L = serac.lib()
     assert L.serac_test_inject_timeout(1) == 0
     assert L.serac_test_inject_timeout(0) == 0
+
+
+def test_topk_argument_checks(serac):
+    """serac_topk_pair rejects bad arguments before it touches a device; without a
+    device the workspace query answers 0."""
+    L = serac.lib()
+    buf = ctypes.create_string_buffer(1 << 16)
+    a = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 256
+    out = a + 4096
+    assert L.serac_topk_pair(a, 10, a, 10, 0, out, out, None, a, 256, None) == serac.EINVAL   # k < 1
+    assert L.serac_topk_pair(a, 10, a, 10, 9, out, out, None, a, 256, None) == serac.EINVAL   # k > 8
+    assert L.serac_topk_pair(a, -1, a, 10, 2, out, out, None, a, 256, None) == serac.EINVAL   # n < 0
+    assert L.serac_topk_pair(a, 10, a, 10, 2, None, out, None, a, 256, None) == serac.EINVAL  # no scores
+    assert L.serac_topk_pair(a, 10, a, 10, 2, out, out + 2, None, a, 256, None) == serac.EINVAL  # misaligned
+    assert L.serac_topk_pair(a + 8, 10, a, 10, 2, out, out, None, a, 256, None) == serac.EINVAL  # desc alignment
+    assert L.serac_topk_pair(a, 10, a, 10, 2, out, out, out + 1, a, 256, None) == serac.EINVAL  # status alignment
+    import torch
+    if not torch.cuda.is_available():
+        assert serac.topk_workspace_size(100, 100, 4) == 0

@@ -26,7 +26,8 @@ EXPORTS = ("serac_default_params", "serac_pair_workspace_size", "match_pair",
            "match_batch_workspace_size", "match_batch", "serac_scores",
            "serac_set_profile_events", "serac_device_check", "serac_last_launch_count",
            "serac_schedule_describe", "serac_status_str", "match_pair_noalloc",
-           "serac_last_cuda_error", "serac_test_inject_timeout")
+           "serac_last_cuda_error", "serac_test_inject_timeout", "serac_topk_workspace_size",
+           "serac_topk_pair")
 
 
 class SeracError(RuntimeError):
@@ -85,6 +86,9 @@ def lib() -> ctypes.CDLL:
         L.serac_status_str.restype = ctypes.c_char_p
         L.match_pair_noalloc.argtypes = [P, i32, P, i32, ctypes.POINTER(Params), ctypes.POINTER(_Out), P]
         L.serac_test_inject_timeout.argtypes = [ctypes.c_int]
+        L.serac_topk_workspace_size.argtypes = [i32, i32, i32]
+        L.serac_topk_workspace_size.restype = sz
+        L.serac_topk_pair.argtypes = [P, i32, P, i32, i32, P, P, P, P, sz, P]
         _lib_handle = L
     return _lib_handle
 
@@ -242,6 +246,48 @@ def match_pair_noalloc(a: torch.Tensor, b: torch.Tensor, params: Optional[Params
                                   ctypes.byref(c), _stream_ptr(stream))
     _check(st, "match_pair_noalloc")
     return o
+
+
+MAX_TOPK = 8
+
+
+@dataclass
+class TopkOutput:
+    """Row top-k of one pair: scores and index (n_a, k) int32 -- row i's k best columns,
+    score descending then lower column first, padded (0, -1) -- and `status` (1,) int32:
+    OK, or ETIMEOUT when a bounded wait inside a kernel ran out."""
+    scores: torch.Tensor
+    index: torch.Tensor
+    status: torch.Tensor
+
+
+def topk_workspace_size(n_a: int, n_b: int, k: int) -> int:
+    """Workspace bytes of topk_pair on the current device (0 on bad arguments)."""
+    return int(lib().serac_topk_workspace_size(int(n_a), int(n_b), int(k)))
+
+
+def topk_pair(a: torch.Tensor, b: torch.Tensor, k: int, *, workspace_t: Optional[torch.Tensor] = None,
+              stream=None, out: Optional[TopkOutput] = None, host_out: bool = False) -> TopkOutput:
+    """Row top-k (guided matching candidates) of a against b, asynchronously: for every
+    row of a, its k (1..8) highest-scoring rows of b.  a and b may be CUDA or pinned
+    host tensors; host_out=True puts the outputs in pinned host memory."""
+    a, b = _desc(a, "a"), _desc(b, "b")
+    n_a, n_b = a.shape[0], b.shape[0]
+    dev = a.device if a.is_cuda else (b.device if b.is_cuda else torch.device("cuda", torch.cuda.current_device()))
+    if not 1 <= int(k) <= MAX_TOPK:
+        raise SeracError(EINVAL, f"topk_pair (k = {k})")
+    ws = workspace_t if workspace_t is not None else workspace(topk_workspace_size(n_a, n_b, k), dev)
+    if out is None:
+        def buf(shape):
+            if host_out:
+                return torch.empty(shape, dtype=torch.int32, pin_memory=True)
+            return torch.empty(shape, dtype=torch.int32, device=dev)
+        out = TopkOutput(scores=buf((max(n_a, 1), int(k))), index=buf((max(n_a, 1), int(k))), status=buf((1,)))
+    st = lib().serac_topk_pair(a.data_ptr(), n_a, b.data_ptr(), n_b, int(k), out.scores.data_ptr(),
+                               out.index.data_ptr(), out.status.data_ptr(), ws.data_ptr(), ws.numel(),
+                               _stream_ptr(stream))
+    _check(st, "topk_pair")
+    return out
 
 
 def _pairs_struct(pairs: Sequence):

@@ -11,7 +11,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libserac_gb300.so")
-SOURCES = ["api.cu", "fused.cu", "finish.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "fused.cu", "finish.cu", "noalloc.cu", "topk.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")

@@ -433,7 +433,7 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
       const bool prof = first_fused && g_ev_begin && g_ev_end;
       if (prof)
         SERAC_TRY_CUDA(cudaEventRecordWithFlags(g_ev_begin, static_cast<cudaStream_t>(stream), cudaEventRecordExternal));
-      SERAC_TRY_CUDA(static_cast<cudaError_t>(launch_fused(fp, &map, dump != nullptr, stream)));
+      SERAC_TRY_CUDA(static_cast<cudaError_t>(launch_fused(fp, &map, dump ? MODE_DUMP : MODE_TOP2, stream)));
       ++g_last_launches;
       if (prof)
         SERAC_TRY_CUDA(cudaEventRecordWithFlags(g_ev_end, static_cast<cudaStream_t>(stream), cudaEventRecordExternal));
@@ -484,6 +484,114 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
       ++g_last_launches;
     }
   }
+  return SERAC_OK;
+}
+
+// ------------------------------------------------------------------ row top-k
+// One row problem (A's rows against B) on the persistent fused kernel in a top-k mode,
+// then the merge of its segment lists.  Workspace: the error word, A and B staged as
+// bf16, the lists (slots x 4 quarters x K keys per row, slots = the most pieces that
+// cover one row tile).
+struct TopkPlan {
+  int K = 4, grid = 1, slots = 0, ldl = 0;
+  int64_t tiles = 0;
+  size_t off_err = 0, off_staged = 0, off_lists = 0, total = 0;
+  int64_t staged_rows = 0;
+};
+
+int topk_plan(int32_t n_a, int32_t n_b, int32_t k, int sms, TopkPlan& tp) {
+  if (k < 1 || k > MAX_TOPK || n_a < 0 || n_b < 0 || n_a > SERAC_MAX_N || n_b > SERAC_MAX_N) return SERAC_EINVAL;
+  tp.K = k <= 4 ? MODE_TOPK4 : MODE_TOPK8;
+  tp.tiles = problem_tiles(n_a, n_b);
+  tp.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({static_cast<int64_t>(sms), tp.tiles, MAX_GRID})));
+  tp.ldl = static_cast<int>(round_up(std::max(n_a, 1), BM));
+  tp.slots = 0;
+  const int64_t ct = col_tiles(n_b);
+  for (int64_t rt = 0; tp.tiles > 0 && rt < row_tiles(n_a); ++rt) {
+    const int64_t t0 = rt * ct, t1 = std::min(tp.tiles, t0 + ct);
+    tp.slots = std::max(tp.slots, piece_of(t1 - 1, tp.tiles, tp.grid) - piece_of(t0, tp.tiles, tp.grid) + 1);
+  }
+  tp.staged_rows = round_up(n_a, PAD_ROWS) + round_up(n_b, PAD_ROWS);
+  size_t off = 0;
+  tp.off_err = off;
+  off = align_up(off + 256);
+  tp.off_staged = off;
+  off = align_up(off + static_cast<size_t>(tp.staged_rows) * KDIM * 2);
+  tp.off_lists = off;
+  off = align_up(off + static_cast<size_t>(tp.slots) * 4 * tp.K * tp.ldl * 8);
+  tp.total = off;
+  return SERAC_OK;
+}
+
+static_assert(MAX_TOPK == SERAC_MAX_TOPK, "one top-k limit");
+
+int run_topk(const uint8_t* a, int32_t n_a, const uint8_t* b, int32_t n_b, int32_t k, int32_t* scores,
+             int32_t* index, int32_t* status, void* workspace, size_t ws_bytes, void* stream) {
+  g_last_launches = 0;
+  int sms = 0;
+  int st = device_info(&sms);
+  if (st != SERAC_OK) return st;
+  TopkPlan tp;
+  st = topk_plan(n_a, n_b, k, sms, tp);
+  if (st != SERAC_OK) return st;
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < tp.total) return SERAC_EWORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* err = reinterpret_cast<int32_t*>(ws + tp.off_err);
+  uint16_t* staged = reinterpret_cast<uint16_t*>(ws + tp.off_staged);
+  CUtensorMap map;
+  st = encode_staged_map(&map, staged, tp.staged_rows);
+  if (st != SERAC_OK) return st;
+  // staging (clears the error word); the lists need no clearing: the merge reads only
+  // the slots the row's segments write
+  StageParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  sp.staged = staged;
+  sp.err = err;
+  sp.zero_blocks = 1;  // its first block clears the error word (nothing else to clear)
+  int64_t max_chunks = 0;
+  const int32_t b_row0 = static_cast<int32_t>(round_up(n_a, PAD_ROWS));
+  if (n_a > 0) sp.images[sp.n_images++] = StageImage{a, n_a, 0};
+  if (n_b > 0) sp.images[sp.n_images++] = StageImage{b, n_b, b_row0};
+  for (int i = 0; i < sp.n_images; ++i)
+    max_chunks = std::max<int64_t>(max_chunks, round_up(sp.images[i].n, PAD_ROWS) * (KDIM / 16));
+  SERAC_TRY_CUDA(static_cast<cudaError_t>(launch_stage(sp, max_chunks, stream, false)));
+  ++g_last_launches;
+  unsigned long long* lists = reinterpret_cast<unsigned long long*>(ws + tp.off_lists);
+  if (tp.tiles > 0) {
+    FusedParams fp;
+    std::memset(&fp, 0, sizeof(fp));
+    fp.grid = tp.grid;
+    fp.err = err;
+    fp.key_mult = 256u;
+    fp.no_copies = g_inject_no_copies ? 1 : 0;
+    g_inject_no_copies = false;
+    FusedPair& f = fp.pairs[0];
+    f.a_row0 = 0;
+    f.b_row0 = b_row0;
+    f.n_a = n_a;
+    f.n_b = n_b;
+    f.npieces = static_cast<int32_t>(std::min<int64_t>(tp.grid, tp.tiles));
+    f.offset = 0;
+    f.ldl = tp.ldl;
+    f.keys = lists;
+    fp.n_pairs = 1;
+    SERAC_TRY_CUDA(static_cast<cudaError_t>(launch_fused(fp, &map, tp.K, stream)));
+    ++g_last_launches;
+  }
+  TopkMergeParams mp;
+  std::memset(&mp, 0, sizeof(mp));
+  mp.lists = lists;
+  mp.n_a = n_a;
+  mp.n_b = n_b;
+  mp.ldl = tp.ldl;
+  mp.grid = tp.grid;
+  mp.k = k;
+  mp.scores = scores;
+  mp.index = index;
+  mp.status = status;
+  mp.err = err;
+  SERAC_TRY_CUDA(static_cast<cudaError_t>(launch_topk_merge(mp, tp.K, stream)));
+  ++g_last_launches;
   return SERAC_OK;
 }
 
@@ -588,6 +696,30 @@ int serac_scores(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b, int3
   serac_default_params(&dummy, 0.8f, 0.7f);
   return run(&pr, 1, &dummy, nullptr, scores ? scores : reinterpret_cast<int32_t*>(16), workspace,
              workspace_bytes, cuda_stream);
+}
+
+size_t serac_topk_workspace_size(int32_t n_a, int32_t n_b, int32_t k) {
+  int sms = 0;
+  if (device_info(&sms) != SERAC_OK) return 0;
+  TopkPlan tp;
+  if (topk_plan(n_a, n_b, k, sms, tp) != SERAC_OK) return 0;
+  return tp.total;
+}
+
+int serac_topk_pair(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b, int32_t n_b, int32_t k,
+                    int32_t* scores, int32_t* index, int32_t* status, void* workspace, size_t workspace_bytes,
+                    void* cuda_stream) {
+  serac_pair pr;
+  pr.a = desc_a;
+  pr.n_a = n_a;
+  pr.b = desc_b;
+  pr.n_b = n_b;
+  int st = check_pairs(&pr, 1);
+  if (st != SERAC_OK) return st;
+  if (k < 1 || k > SERAC_MAX_TOPK) return SERAC_EINVAL;
+  if (n_a > 0 && (!scores || !index || !aligned(scores, 4) || !aligned(index, 4))) return SERAC_EINVAL;
+  if (status && !aligned(status, 4)) return SERAC_EINVAL;
+  return run_topk(desc_a, n_a, desc_b, n_b, k, scores, index, status, workspace, workspace_bytes, cuda_stream);
 }
 
 int serac_set_profile_events(void* ev_begin, void* ev_end) {

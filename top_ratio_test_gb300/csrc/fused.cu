@@ -75,15 +75,16 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
-// Where a CTA stands in its work: problem p, the next tile t of its piece of that
-// problem and the piece's end (tiles numbered row-major within the problem).
+// Where a CTA stands in its work: problem p, its piece k of that problem, the next
+// tile t of the piece and the piece's end (tiles numbered row-major within the problem).
 struct Cursor {
-  int p, t, tend;
+  int p, k, t, tend;
 };
 
-// One segment: row tile rt of problem p against the column tiles [ct0, ct1).
+// One segment: row tile rt of problem p against the column tiles [ct0, ct1), part of
+// piece k.
 struct Segment {
-  int p, rt, ct0, ct1;
+  int p, k, rt, ct0, ct1;
 };
 
 // Advances `cur` by one segment; false once the CTA has no work left.  Piece k of a
@@ -99,11 +100,13 @@ __device__ __forceinline__ bool next_segment(const FusedParams& P, Cursor& cur, 
     if (k >= fp.npieces) continue;
     const int tiles = ((fp.n_a + BM - 1) / BM) * ((fp.n_b + BN - 1) / BN);
     const int q = tiles / P.grid, r = tiles - q * P.grid;
+    cur.k = k;
     cur.t = k * q + min(k, r);
     cur.tend = cur.t + q + (k < r ? 1 : 0);
   }
   const int ct_total = (P.pairs[cur.p].n_b + BN - 1) / BN;
   g.p = cur.p;
+  g.k = cur.k;
   g.rt = cur.t / ct_total;
   g.ct0 = cur.t - g.rt * ct_total;
   g.ct1 = min(ct_total, g.ct0 + (cur.tend - cur.t));
@@ -159,7 +162,127 @@ __device__ __forceinline__ unsigned long long key64(uint32_t k, uint32_t base) {
   return (static_cast<unsigned long long>(s) << 32) | (0xFFFFFFFFu - idx);
 }
 
-template <bool DUMP>
+// ---- row top-k (k = 4 or 8): sorting networks on distinct keys, largest first
+__device__ __forceinline__ void ce(float& a, float& b) {  // a <- max, b <- min
+  const float hi = fmaxf(a, b), lo = fminf(a, b);
+  a = hi;
+  b = lo;
+}
+__device__ __forceinline__ void ce64(unsigned long long& a, unsigned long long& b) {
+  const unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+// Sorts x[0..K) in descending order (K = 4: 5 compare-exchanges; K = 8: Batcher's
+// odd-even merge sort, 19).
+template <int K>
+__device__ __forceinline__ void sort_net(float* x) {
+  if constexpr (K == 4) {
+    ce(x[0], x[1]); ce(x[2], x[3]); ce(x[0], x[2]); ce(x[1], x[3]); ce(x[1], x[2]);
+  } else {
+    ce(x[0], x[1]); ce(x[2], x[3]); ce(x[4], x[5]); ce(x[6], x[7]);
+    ce(x[0], x[2]); ce(x[1], x[3]); ce(x[4], x[6]); ce(x[5], x[7]);
+    ce(x[1], x[2]); ce(x[5], x[6]);
+    ce(x[0], x[4]); ce(x[1], x[5]); ce(x[2], x[6]); ce(x[3], x[7]);
+    ce(x[2], x[4]); ce(x[3], x[5]);
+    ce(x[1], x[2]); ce(x[3], x[4]); ce(x[5], x[6]);
+  }
+}
+// a <- the K largest of a and b, both sorted descending: the larger of a[i] and
+// b[K-1-i] are the K largest and form a bitonic sequence, which a bitonic merge sorts.
+__device__ __forceinline__ float max_of(float a, float b) { return fmaxf(a, b); }
+__device__ __forceinline__ unsigned long long max_of(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
+__device__ __forceinline__ void cex(float& a, float& b) { ce(a, b); }
+__device__ __forceinline__ void cex(unsigned long long& a, unsigned long long& b) { ce64(a, b); }
+template <int K, typename T>
+__device__ __forceinline__ void merge_top(T* a, const T* b) {
+#pragma unroll
+  for (int i = 0; i < K; ++i) a[i] = max_of(a[i], b[K - 1 - i]);
+#pragma unroll
+  for (int w = K / 2; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < K; ++i)
+      if ((i & w) == 0) cex(a[i], a[i + w]);
+}
+// The K largest tile keys (s << 8 | 255 - column in the tile) of one 32-column half,
+// sorted descending: keys by one multiply-add each, sorted groups of K, then merges.
+template <int K>
+__device__ __forceinline__ void half_topk(const uint32_t (&v)[32], uint32_t key_mult, uint32_t chb, float (&t)[K]) {
+  float x[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(mad_lo(v[k], key_mult, 31u - k));
+#pragma unroll
+  for (int gi = 0; gi < 32 / K; ++gi) sort_net<K>(x + gi * K);
+#pragma unroll
+  for (int gi = 1; gi < 32 / K; ++gi) merge_top<K>(x, x + gi * K);
+#pragma unroll
+  for (int i = 0; i < K; ++i) t[i] = __uint_as_float(__float_as_uint(x[i]) | chb);
+}
+
+// The epilogue of the row top-k modes: per segment, each row's K largest 64-bit keys
+// over this warp's quarter of the columns, kept sorted in registers across the tiles
+// and written to the segment's list (topk_list_index) at the segment's end.
+template <int K>
+__device__ __forceinline__ void topk_epilogue(const FusedParams& P, uint32_t tmem_base, uint64_t* t_full,
+                                              uint64_t* t_empty, volatile int* abort_flag, int warp, int lane) {
+  const int e = warp - 2;    // 0..15
+  const int q = warp & 3;    // TMEM lane quadrant this warp may read
+  const int qt = e >> 2;     // which 64-column quarter of the tile
+  const uint32_t rl = static_cast<uint32_t>(q * 32 + lane);
+  const uint32_t key_mult = P.key_mult;
+  uint32_t tcount = 0;
+  bool ok = true;
+  Cursor cur{-1, 0, 0, 0};
+  Segment g;
+  while (next_segment(P, cur, g)) {
+    const FusedPair& fp = P.pairs[g.p];
+    unsigned long long R[K];  // the row's K best keys of the segment, descending; 0 = empty
+#pragma unroll
+    for (int j = 0; j < K; ++j) R[j] = 0ull;
+    for (int ct = g.ct0; ct < g.ct1; ++ct, ++tcount) {
+      const uint32_t acc = tcount & 1u, aph = (tcount >> 1) & 1u;
+      {
+        const bool w = mbar_wait(&t_full[acc], aph, abort_flag, P.err, ERR_TIMEOUT_EPILOGUE, WAIT_LIMIT_NS);
+        if (!__all_sync(0xffffffffu, w)) ok = false;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + qt * 64;
+      // the two 32-column halves one after the other (32 values live at a time); the
+      // buffer goes back to the MMA once the second is in registers.  Half index
+      // (31 - k) -> tile-local 255 - (64 qt + 32 c + k).
+      float t[K], u[K];
+      {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr, v);
+        tmem_wait_ld();
+        half_topk<K>(v, key_mult, static_cast<uint32_t>(7 - 2 * qt) << 5, t);
+      }
+      {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + 32, v);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&t_empty[acc]);
+        half_topk<K>(v, key_mult, static_cast<uint32_t>(6 - 2 * qt) << 5, u);
+      }
+      merge_top<K>(t, u);  // the tile's K largest
+      unsigned long long y[K];
+#pragma unroll
+      for (int j = 0; j < K; ++j) y[j] = key64(__float_as_uint(t[j]), static_cast<uint32_t>(ct * BN));
+      merge_top<K>(R, y);
+    }
+    const int i = g.rt * BM + static_cast<int>(rl);
+    if (ok && i < fp.n_a) {
+      const int ct_total = (fp.n_b + BN - 1) / BN;
+      const int64_t tiles = static_cast<int64_t>((fp.n_a + BM - 1) / BM) * ct_total;
+      const int slot = g.k - piece_of(static_cast<int64_t>(g.rt) * ct_total, tiles, P.grid);
+#pragma unroll
+      for (int j = 0; j < K; ++j) fp.keys[topk_list_index(slot, qt, j, K, fp.ldl, i)] = R[j];
+    }
+  }
+}
+
+template <int MODE>
 __global__ void __launch_bounds__(FUSED_THREADS, 1)
     fused_top2_kernel(const __grid_constant__ FusedParams P, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ uint8_t smem_raw[];
@@ -230,7 +353,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     if (lane == 0 && !P.no_copies) {
       uint32_t bcount = 0, nseg = 0;
       bool ok = true;
-      Cursor cur{-1, 0, 0};
+      Cursor cur{-1, 0, 0, 0};
       Segment g;
       for (; ok && next_segment(P, cur, g); ++nseg) {
         const FusedPair& fp = P.pairs[g.p];
@@ -270,7 +393,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
       const uint64_t a_bias = plain_kmajor_desc(bias_addr, 128, 0);
       const uint64_t b_bias = plain_kmajor_desc(bias_addr + 256, 128, 0);
       bool ok = true;
-      Cursor cur{-1, 0, 0};
+      Cursor cur{-1, 0, 0, 0};
       Segment g;
       for (; ok && next_segment(P, cur, g); ++nseg) {
         if (!mbar_wait(a_full, nseg & 1u, abort_flag, P.err, ERR_TIMEOUT_MMA, WAIT_LIMIT_NS)) break;
@@ -304,8 +427,11 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
       while (!mbar_try_wait(drain, 0) && global_ns() - t0 < WAIT_LIMIT_NS) {
       }
     }
+  } else if constexpr (MODE >= MODE_TOPK4) {
+    topk_epilogue<MODE>(P, tmem_base, t_full, t_empty, abort_flag, warp, lane);
   } else {
     // ------------------------------------------------------------ epilogue
+    constexpr bool DUMP = MODE == MODE_DUMP;
     const int e = warp - 2;       // 0..15
     const int q = warp & 3;       // TMEM lane quadrant this warp may read
     const int qt = e >> 2;        // which 64-column quarter of the tile
@@ -320,7 +446,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     // returning atomic's latency overlaps the next segment
     unsigned long long* pend_ptr = nullptr;
     unsigned long long pend_old = 0ull, pend_x1 = 0ull;
-    Cursor cur{-1, 0, 0};
+    Cursor cur{-1, 0, 0, 0};
     Segment g;
     while (next_segment(P, cur, g)) {
       const FusedPair& fp = P.pairs[g.p];
@@ -428,17 +554,15 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
 
 int fused_smem_bytes() { return SMEM_TOTAL; }
 
-int launch_fused(const FusedParams& p, const void* tmap, bool dump, void* stream) {
+namespace {
+template <int MODE>
+cudaError_t launch_mode(const FusedParams& p, const CUtensorMap& map, void* stream) {
   // the opt-in to more than 48 KB of dynamic shared memory is an attribute of the
   // function on the current device: set it on every launch (cheap), so that every
   // device the caller makes current gets it
-  cudaError_t e = dump ? cudaFuncSetAttribute(fused_top2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              SMEM_TOTAL)
-                       : cudaFuncSetAttribute(fused_top2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              SMEM_TOTAL);
-  if (e != cudaSuccess) return static_cast<int>(e);
-  CUtensorMap map;
-  memcpy(&map, tmap, sizeof(map));
+  cudaError_t e =
+      cudaFuncSetAttribute(fused_top2_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(FUSED_THREADS);
@@ -449,9 +573,20 @@ int launch_fused(const FusedParams& p, const void* tmap, bool dump, void* stream
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = dump ? cudaLaunchKernelEx(&cfg, fused_top2_kernel<true>, p, map)
-           : cudaLaunchKernelEx(&cfg, fused_top2_kernel<false>, p, map);
-  return static_cast<int>(e);
+  return cudaLaunchKernelEx(&cfg, fused_top2_kernel<MODE>, p, map);
+}
+}  // namespace
+
+int launch_fused(const FusedParams& p, const void* tmap, int mode, void* stream) {
+  CUtensorMap map;
+  memcpy(&map, tmap, sizeof(map));
+  switch (mode) {
+    case MODE_TOP2: return static_cast<int>(launch_mode<MODE_TOP2>(p, map, stream));
+    case MODE_DUMP: return static_cast<int>(launch_mode<MODE_DUMP>(p, map, stream));
+    case MODE_TOPK4: return static_cast<int>(launch_mode<MODE_TOPK4>(p, map, stream));
+    case MODE_TOPK8: return static_cast<int>(launch_mode<MODE_TOPK8>(p, map, stream));
+    default: return static_cast<int>(cudaErrorInvalidValue);
+  }
 }
 
 }  // namespace serac

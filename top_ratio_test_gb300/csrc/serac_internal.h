@@ -50,8 +50,45 @@ struct FusedPair {
   int32_t npieces;     // pieces the problem's tiles are cut into (<= grid)
   int32_t offset;      // piece k goes to CTA (offset + k) mod grid
   int32_t transposed;  // score dump only: rows are the pair's B (write S[col][row])
-  int32_t pad_;
-  unsigned long long* keys;  // [n_a][2] row keys of this problem (rowkeys or colkeys of the pair)
+  int32_t ldl;         // row top-k only: row stride of the segment lists (n_a rounded up to BM)
+  unsigned long long* keys;  // [n_a][2] row keys of this problem (rowkeys or colkeys of the pair);
+                             // row top-k: the segment lists (see topk_list_index)
+};
+
+// Epilogue modes of the fused kernel.
+constexpr int MODE_TOP2 = 0;   // row top-2 of every problem, merged into the global keys
+constexpr int MODE_DUMP = 1;   // the score matrix itself (small pairs, tests only)
+constexpr int MODE_TOPK4 = 4;  // row top-4 per segment, written to segment lists
+constexpr int MODE_TOPK8 = 8;  // row top-8 per segment, written to segment lists
+constexpr int MAX_TOPK = 8;
+
+// The piece that holds tile t when T tiles are dealt to `grid` CTAs (T / grid tiles
+// per piece and one more for the first T mod grid pieces).
+__host__ __device__ inline int32_t piece_of(int64_t t, int64_t T, int32_t grid) {
+  const int64_t q = T / grid, r = T % grid;
+  if (t < r * (q + 1)) return static_cast<int32_t>(t / (q + 1));
+  return static_cast<int32_t>(r + (t - r * (q + 1)) / q);
+}
+
+// Row top-k lists.  Every segment of a row problem (one piece's run of column tiles on
+// one row tile) writes, per row and per 64-column quarter of the tiles, the K best
+// 64-bit keys it saw, in descending order.  The segments of row tile rt are the
+// pieces piece_of(rt C) .. piece_of(min(T, (rt + 1) C) - 1), C = column tiles; the
+// piece's position in that range is its slot.  Key j of (slot, quarter) of row i sits
+// at ((slot * 4 + quarter) * K + j) * ldl + i: consecutive rows are adjacent, so a
+// warp's writes and the merge kernel's reads are coalesced.
+__host__ __device__ inline int64_t topk_list_index(int32_t slot, int32_t quarter, int32_t j, int32_t K, int32_t ldl,
+                                                   int32_t row) {
+  return (static_cast<int64_t>(slot * 4 + quarter) * K + j) * ldl + row;
+}
+
+struct TopkMergeParams {
+  const unsigned long long* lists;
+  int32_t n_a, n_b, ldl, grid, k;  // k <= K: entries written per row
+  int32_t* scores;                 // [n_a][k]
+  int32_t* index;                  // [n_a][k]
+  int32_t* status;                 // SERAC_OK, or SERAC_ETIMEOUT when a kernel wait ran out (may be NULL)
+  const int32_t* err;
 };
 
 // Final top-2 of a row or column as two 64-bit keys (best, second):
@@ -120,7 +157,8 @@ struct FinishParams {
 
 // launchers (defined in fused.cu / finish.cu); return a cudaError_t value
 int launch_stage(const StageParams& p, int64_t max_chunks, void* stream, bool beside_fused);
-int launch_fused(const FusedParams& p, const void* tmap, bool dump, void* stream);
+int launch_fused(const FusedParams& p, const void* tmap, int mode, void* stream);
+int launch_topk_merge(const TopkMergeParams& p, int K, void* stream);
 int launch_match(const FinishParams& p, void* stream);
 int fused_smem_bytes();
 

@@ -1,0 +1,82 @@
+// Row top-k (guided matching): the merge of the segment lists.
+//
+// The fused kernel's top-k modes leave, for every segment of the row problem and every
+// 64-column quarter of its tiles, each row's K largest 64-bit keys (score << 32 |
+// ~column) in descending order (serac_internal.h, topk_list_index).  This kernel takes,
+// for one row per thread, the lists of the segments of its row tile, keeps the K
+// largest keys of their union (keys are distinct, so the order of merges is free) and
+// writes the first k as (score, column), a missing entry or a zero score as (0, -1):
+// the candidate list of the "SERAC" page's "Exactness" order (score descending, lower
+// index first, the zero floor) cut after k instead of after two.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+#include "serac.h"
+#include "serac_internal.h"
+
+namespace serac {
+namespace {
+
+constexpr int MERGE_THREADS = 128;
+
+template <int K>
+__global__ void __launch_bounds__(MERGE_THREADS) topk_merge_kernel(const TopkMergeParams p) {
+  grid_dep_wait();  // the fused kernel's lists and error word
+  const int i = static_cast<int>(blockIdx.x) * MERGE_THREADS + static_cast<int>(threadIdx.x);
+  if (i == 0 && p.status) *p.status = *p.err ? SERAC_ETIMEOUT : SERAC_OK;
+  if (i >= p.n_a) return;
+  unsigned long long top[K];
+#pragma unroll
+  for (int j = 0; j < K; ++j) top[j] = 0ull;
+  if (p.n_b > 0) {
+    const int ct_total = (p.n_b + BN - 1) / BN;
+    const int64_t tiles = static_cast<int64_t>((p.n_a + BM - 1) / BM) * ct_total;
+    const int rt = i / BM;
+    const int64_t t0 = static_cast<int64_t>(rt) * ct_total;
+    const int64_t t1 = t0 + ct_total < tiles ? t0 + ct_total : tiles;
+    const int slots = piece_of(t1 - 1, tiles, p.grid) - piece_of(t0, tiles, p.grid) + 1;
+    for (int slot = 0; slot < slots; ++slot)
+      for (int quarter = 0; quarter < 4; ++quarter)
+        for (int j = 0; j < K; ++j) {
+          unsigned long long x = p.lists[topk_list_index(slot, quarter, j, K, p.ldl, i)];
+          if (x <= top[K - 1]) break;  // each list is descending: nothing after x enters
+          // insert x into the descending list: each slot keeps the larger, passes the other on
+#pragma unroll
+          for (int s = 0; s < K; ++s) {
+            const unsigned long long hi = top[s] > x ? top[s] : x;
+            x = top[s] > x ? x : top[s];
+            top[s] = hi;
+          }
+        }
+  }
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    if (j >= p.k) break;
+    const unsigned long long x = top[j];
+    const int64_t at = static_cast<int64_t>(i) * p.k + j;
+    p.scores[at] = x ? static_cast<int32_t>(x >> 32) : 0;
+    p.index[at] = x ? static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(x)) : -1;
+  }
+}
+
+}  // namespace
+
+int launch_topk_merge(const TopkMergeParams& p, int K, void* stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((p.n_a + MERGE_THREADS - 1) / MERGE_THREADS > 0
+                                               ? (p.n_a + MERGE_THREADS - 1) / MERGE_THREADS
+                                               : 1));
+  cfg.blockDim = dim3(MERGE_THREADS);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (K == 4) return static_cast<int>(cudaLaunchKernelEx(&cfg, topk_merge_kernel<4>, p));
+  if (K == 8) return static_cast<int>(cudaLaunchKernelEx(&cfg, topk_merge_kernel<8>, p));
+  return static_cast<int>(cudaErrorInvalidValue);
+}
+
+}  // namespace serac
