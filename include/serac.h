@@ -171,7 +171,7 @@ int serac_topk_pair(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b, i
                     void* cuda_stream);
 
 /* Profiling hook: when both events are non-NULL (cudaEvent_t), every following
- * match_pair / match_batch call made by the calling thread records `ev_begin` just
+ * match_pair / match_batch / serac_topk_pair call made by the calling thread records `ev_begin` just
  * before its first fused GEMM + top-2 launch and `ev_end` just after it, on the
  * call's stream.  NULL, NULL turns it off.  The setting belongs to the calling
  * thread; other threads' calls are not affected. */

@@ -575,8 +575,13 @@ int run_topk(const uint8_t* a, int32_t n_a, const uint8_t* b, int32_t n_b, int32
     f.ldl = tp.ldl;
     f.keys = lists;
     fp.n_pairs = 1;
+    const bool prof = g_ev_begin && g_ev_end;
+    if (prof)
+      SERAC_TRY_CUDA(cudaEventRecordWithFlags(g_ev_begin, static_cast<cudaStream_t>(stream), cudaEventRecordExternal));
     SERAC_TRY_CUDA(static_cast<cudaError_t>(launch_fused(fp, &map, tp.K, stream)));
     ++g_last_launches;
+    if (prof)
+      SERAC_TRY_CUDA(cudaEventRecordWithFlags(g_ev_end, static_cast<cudaStream_t>(stream), cudaEventRecordExternal));
   }
   TopkMergeParams mp;
   std::memset(&mp, 0, sizeof(mp));
