@@ -37,9 +37,14 @@
 // than the final best reaches `second`, the final best never does (keys are unique),
 // whatever the order.
 //
+// The same template serves two more epilogues (MODE): the score dump (the matrix
+// written out, for the exactness and fused == unfused checks) and the row top-k of
+// guided matching (each row's k <= 8 best keys per segment, sorting networks in place
+// of the trees, written to per-segment lists that topk.cu merges).
+//
 // Zero-padded rows and columns score 0 and fall to the zero floor, so ragged tails
 // need no masking.  Every wait is bounded; a timeout sets an error bit that the
-// match kernel reports through the count.
+// match kernel (or the top-k merge) reports.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
