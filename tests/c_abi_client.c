@@ -6,8 +6,10 @@
  *
  * reads nA x 128 and nB x 128 raw uint8 descriptors, matches them with match_pair
  * (device buffers from cudaMalloc, the default stream) and with match_pair_noalloc,
- * checks the argument-error path, and writes to out.bin:
- *   int32 count, int32 matches[count][2], int32 row_top2[nA][4], int32 col_top2[nB][4].
+ * checks the argument-error path, runs the row top-3 (serac_topk_pair), and writes to
+ * out.bin:
+ *   int32 count, int32 matches[count][2], int32 row_top2[nA][4], int32 col_top2[nB][4],
+ *   int32 top3_scores[nA][3], int32 top3_index[nA][3].
  * Exit status 0 on success; the caller compares out.bin with the oracle.
  */
 #include <stdint.h>
@@ -121,12 +123,38 @@ int main(int argc, char** argv) {
   CHECK_CUDA(cudaMemcpy(hm2, matches, (size_t)n * 2 * sizeof(int32_t), cudaMemcpyDeviceToHost));
   if (n && memcmp(hm, hm2, (size_t)n * 2 * sizeof(int32_t)) != 0) return 11;
 
+  /* the row top-3 of the same pair */
+  int32_t *tks = NULL, *tki = NULL, *tst = NULL;
+  void* tws = NULL;
+  const size_t tws_bytes = serac_topk_workspace_size(na, nb, 3);
+  if (tws_bytes == 0) return 13;
+  CHECK_CUDA(cudaMalloc((void**)&tks, (size_t)(na ? na : 1) * 3 * sizeof(int32_t)));
+  CHECK_CUDA(cudaMalloc((void**)&tki, (size_t)(na ? na : 1) * 3 * sizeof(int32_t)));
+  CHECK_CUDA(cudaMalloc((void**)&tst, sizeof(int32_t)));
+  CHECK_CUDA(cudaMalloc(&tws, tws_bytes));
+  if (serac_topk_pair(da, na, db, nb, 9, tks, tki, tst, tws, tws_bytes, NULL) != SERAC_EINVAL) return 14;
+  st = serac_topk_pair(da, na, db, nb, 3, tks, tki, tst, tws, tws_bytes, NULL);
+  if (st != SERAC_OK) {
+    fprintf(stderr, "serac_topk_pair: %s\n", serac_status_str(st));
+    return 15;
+  }
+  CHECK_CUDA(cudaDeviceSynchronize());
+  int32_t tstatus = -99;
+  CHECK_CUDA(cudaMemcpy(&tstatus, tst, sizeof(int32_t), cudaMemcpyDeviceToHost));
+  if (tstatus != SERAC_OK) return 16;
+  int32_t* hks = (int32_t*)malloc((size_t)(na ? na : 1) * 3 * sizeof(int32_t));
+  int32_t* hki = (int32_t*)malloc((size_t)(na ? na : 1) * 3 * sizeof(int32_t));
+  CHECK_CUDA(cudaMemcpy(hks, tks, (size_t)na * 3 * sizeof(int32_t), cudaMemcpyDeviceToHost));
+  CHECK_CUDA(cudaMemcpy(hki, tki, (size_t)na * 3 * sizeof(int32_t), cudaMemcpyDeviceToHost));
+
   FILE* f = fopen(argv[5], "wb");
   if (!f) return 12;
   fwrite(&n, sizeof(int32_t), 1, f);
   fwrite(hm, sizeof(int32_t), (size_t)n * 2, f);
   fwrite(hr, sizeof(int32_t), (size_t)na * 4, f);
   fwrite(hc, sizeof(int32_t), (size_t)nb * 4, f);
+  fwrite(hks, sizeof(int32_t), (size_t)na * 3, f);
+  fwrite(hki, sizeof(int32_t), (size_t)na * 3, f);
   fclose(f);
   printf("%d matches\n", n);
   cudaFree(da);
@@ -136,6 +164,12 @@ int main(int argc, char** argv) {
   cudaFree(row_top2);
   cudaFree(col_top2);
   cudaFree(ws);
+  cudaFree(tks);
+  cudaFree(tki);
+  cudaFree(tst);
+  cudaFree(tws);
+  free(hks);
+  free(hki);
   free(ha);
   free(hb);
   free(hm);

@@ -46,9 +46,17 @@ def test_c_client_matches_oracle(tmp_path, oracle_mod):
     n = int(raw[0])
     na, nb = p.a.shape[0], p.b.shape[0]
     matches = raw[1:1 + 2 * n].reshape(n, 2)
-    row_top2 = raw[1 + 2 * n:1 + 2 * n + 4 * na].reshape(na, 4)
-    col_top2 = raw[1 + 2 * n + 4 * na:].reshape(nb, 4)
+    o = 1 + 2 * n
+    row_top2 = raw[o:o + 4 * na].reshape(na, 4)
+    o += 4 * na
+    col_top2 = raw[o:o + 4 * nb].reshape(nb, 4)
+    o += 4 * nb
+    top3_s = raw[o:o + 3 * na].reshape(na, 3)
+    top3_i = raw[o + 3 * na:].reshape(na, 3)
     ref = oracle_mod.match(p.a, p.b)
     np.testing.assert_array_equal(matches, ref.matches)
     np.testing.assert_array_equal(row_top2, ref.row_top2)
     np.testing.assert_array_equal(col_top2, ref.col_top2)
+    rs, ri = oracle_mod.row_topk(p.a, p.b, 3)
+    np.testing.assert_array_equal(top3_s, rs)
+    np.testing.assert_array_equal(top3_i, ri)
