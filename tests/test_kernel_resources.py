@@ -64,3 +64,11 @@ def test_stage_and_match_kernels_fit_beside_a_fused_cta():
         for k in ks:
             assert k["regs"] <= 32, (name, k)
             assert k.get("spill", 0) == 0, (name, k)
+
+
+def test_topk_merge_kernel_without_spills():
+    rep = _ptxas_report("topk.cu")
+    ks = _entry(rep, "topk_merge_kernel")
+    assert len(ks) == 2, rep   # the K = 4 and K = 8 builds
+    for k in ks:
+        assert k.get("spill", 0) == 0, k
