@@ -67,6 +67,18 @@ def test_topk_ties(serac, oracle_mod, k):
     np.testing.assert_array_equal(ix, ri)
 
 
+@pytest.mark.parametrize("na,nb,k", [(130, 20000, 3), (9000, 300, 8), (256, 65536, 1)])
+def test_topk_extreme_aspect(serac, oracle_mod, na, nb, k):
+    """Few row tiles against many column tiles: a row tile's columns are cut into dozens
+    of pieces (one list slot each); many row tiles against one column tile: one slot."""
+    p = S.make_pair(4, 7, na + nb, na, nb, 0.25, 0.08)
+    sc, ix = _topk(serac, p.a, p.b, k)
+    rows = np.unique(np.concatenate([np.arange(0, na, max(1, na // 64)), [na - 1]])).astype(np.int32)
+    rs, ri = oracle_mod.row_topk(p.a, p.b, k, rows=rows)
+    np.testing.assert_array_equal(sc[rows], rs)
+    np.testing.assert_array_equal(ix[rows], ri)
+
+
 def test_topk2_equals_row_top2(serac):
     p = S.single_pair_2000(0)
     sc, ix = _topk(serac, p.a, p.b, 2)
