@@ -173,13 +173,37 @@ def test_schedule_ragged_and_empty(serac):
 
 
 def test_schedule_balanced_over_many_pairs(serac):
-    # 40 pairs of 1,700 + 1,700 tiles and 40 of 5 + 6 tiles: every CTA within one tile
+    # 40 pairs of 1,700 + 1,700 tiles and 40 of 5 + 6 tiles: mixed sizes stay dealt one
+    # piece per CTA, every CTA within one tile
     sizes = [(6400, 8704), (640, 256)] * 40
     chunks, pieces, npieces, cta = serac.schedule_describe(sizes, 152)
     assert chunks == 1
-    total = sum(_pair_tiles(na, nb) for na, nb in sizes)
-    assert sum(cta) == total
-    assert max(cta) - min(cta) <= 1
+    t = [x for na, nb in sizes for x in (_tiles(na, nb), _tiles(nb, na))]
+    assert npieces == [min(152, x) for x in t]
+    assert sum(cta) == sum(t) and max(cta) - min(cta) <= 1
+
+
+def test_schedule_small_pairs_in_whole_row_tiles(serac):
+    # 128 pairs of 1024 x 1024 (8 row tiles x 4 column tiles per problem): dealt one
+    # piece per row tile -- one segment each -- instead of one tile per CTA
+    sizes = [(1024, 1024)] * 128
+    chunks, pieces, npieces, cta = serac.schedule_describe(sizes, 152)
+    assert npieces == [8] * 256 and pieces == 2048
+    assert sum(cta) == 256 * 32 and max(cta) - min(cta) <= 4
+    # the 66-pair ring of 8192 x 8192: whole rows of 32 tiles, 64 pieces per problem
+    chunks, pieces, npieces, cta = serac.schedule_describe([(8192, 8192)] * 66, 152)
+    assert npieces == [64] * 132 and sum(cta) == 132 * 2048 and max(cta) - min(cta) <= 32
+
+
+def test_schedule_ragged_batch_stays_fine(serac):
+    # pairs of mixed sizes: whole-row pieces would leave the CTAs several per cent
+    # apart, so every problem is dealt one piece per CTA and the loads stay within one
+    import sift_synth as S
+    sizes = [(int(a), int(b)) for a, b in S.ragged_sizes(0)[:128]]
+    chunks, pieces, npieces, cta = serac.schedule_describe(sizes, 152)
+    t = [x for na, nb in sizes for x in (_tiles(na, nb), _tiles(nb, na))]
+    assert npieces == [min(152, x) for x in t]
+    assert sum(cta) == sum(t) and max(cta) - min(cta) <= 1
 
 
 def test_schedule_large_batch_chunks(serac):
@@ -187,8 +211,8 @@ def test_schedule_large_batch_chunks(serac):
     chunks, pieces, npieces, cta = serac.schedule_describe(sizes, 152)
     # at most 128 pairs per launch chunk (their tables travel as kernel parameters)
     assert chunks == 3
-    assert npieces[0] == 152 and pieces == 2 * 128 * 152
-    assert sum(cta) == 128 * 2 * 2048 and max(cta) - min(cta) <= 1
+    assert npieces[:256] == [64] * 256 and pieces == 256 * 64
+    assert sum(cta) == 128 * 2 * 2048 and max(cta) - min(cta) <= 32
 
 
 def test_timeout_hook_is_host_only(serac):

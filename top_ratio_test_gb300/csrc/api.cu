@@ -153,22 +153,73 @@ int chunk_grid(const Chunk& ch, int sms) {
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({static_cast<int64_t>(sms), ch.tiles, MAX_GRID})));
 }
 
-// Tiles of piece k when T tiles are dealt to `grid` CTAs: T / grid each, and one
-// more for the first T mod grid pieces.
-int64_t piece_tiles(int64_t t, int grid, int k) { return t / grid + (k < t % grid ? 1 : 0); }
+// Tiles of piece k when T tiles are dealt to n pieces: T / n each, and one more for
+// the first T mod n pieces.
+int64_t piece_tiles(int64_t t, int n, int k) { return t / n + (k < t % n ? 1 : 0); }
 
-// Pieces per problem (min(grid, tiles)) and the CTA of each problem's first piece,
-// for the 2 (p1 - p0) problems of a chunk.  The pieces that carry one tile more go to
-// the CTAs after those that took the previous problem's, so over a chunk every CTA gets
-// the same number of tiles within one.
+// Column tiles of problem k of a chunk (a row tile's run of tiles).
+int64_t chunk_problem_cols(const serac_pair* pairs, int p0, int problem) {
+  const serac_pair& pr = pairs[p0 + problem / 2];
+  return col_tiles((problem & 1) ? pr.n_a : pr.n_b);
+}
+
+// A segment start (the row tile's load, the pipeline refilling, the row's merge into
+// the global keys) costs about half a tile of work; whole-row dealing is taken only
+// when this cost model puts it more than 2 % ahead (the model is approximate, and the
+// whole-row dealing spreads the CTAs' loads by up to a piece).
+constexpr double SEGMENT_COST_TILES = 0.5;
+constexpr double ROWS_MARGIN = 0.98;
+
+// Pieces per problem and the CTA of each problem's first piece, for the 2 (p1 - p0)
+// problems of a chunk.  Two dealings are costed (per CTA: its tiles plus
+// SEGMENT_COST_TILES per segment; the chunk costs its busiest CTA):
+//   * fine: every problem cut into min(grid, T) pieces, i.e. one per CTA for a large
+//     problem; over a chunk the CTAs' tiles differ by at most one (the pieces with a
+//     tile more go to the CTAs after those that took the previous problem's);
+//   * rows: pieces of S tiles, S = the chunk's tiles over 4 per CTA but at most one
+//     row tile's run of column tiles, so that a chunk with far more work than CTAs is
+//     dealt in whole row tiles (one segment each, no row split over CTAs); consecutive
+//     problems' pieces go round the CTAs.
+// A single large pair costs the same both ways and stays fine, as do batches of mixed
+// sizes; batches of equal pairs -- small ones (one-tile segments when dealt fine) most
+// of all -- go rows.
 void plan_pieces(const serac_pair* pairs, const Chunk& ch, int grid, int32_t* npieces, int32_t* offset) {
-  int off = 0;
-  for (int k = 0; k < 2 * (ch.p1 - ch.p0); ++k) {
-    const int64_t t = chunk_problem_tiles(pairs, ch.p0, k);
-    npieces[k] = static_cast<int>(std::min<int64_t>(grid, t));
-    offset[k] = off;
-    off = static_cast<int>((off + t % grid) % grid);
+  const int nprob = 2 * (ch.p1 - ch.p0);
+  std::vector<int64_t> t(nprob), c(nprob);
+  for (int k = 0; k < nprob; ++k) {
+    t[k] = chunk_problem_tiles(pairs, ch.p0, k);
+    c[k] = chunk_problem_cols(pairs, ch.p0, k);
   }
+  const int64_t s_cap = std::max<int64_t>(1, ch.tiles / (static_cast<int64_t>(grid) * 4));
+  std::vector<double> load(grid);
+  auto deal = [&](bool rows, int32_t* np, int32_t* off) {
+    std::fill(load.begin(), load.end(), 0.0);
+    int o = 0;
+    for (int k = 0; k < nprob; ++k) {
+      np[k] = 0;
+      off[k] = o;
+      if (t[k] == 0) continue;
+      const int64_t s = rows ? std::max<int64_t>(1, std::min(c[k], s_cap)) : 1;
+      const int n = static_cast<int>(std::min<int64_t>(grid, (t[k] + s - 1) / s));
+      np[k] = n;
+      const int64_t q = t[k] / n, r = t[k] % n;
+      for (int i = 0; i < n; ++i) {
+        const int64_t t0 = i * q + std::min<int64_t>(i, r), len = q + (i < r ? 1 : 0);
+        const int64_t segs = (t0 % c[k] + len + c[k] - 1) / c[k];
+        load[(o + i) % grid] += static_cast<double>(len) + SEGMENT_COST_TILES * static_cast<double>(segs);
+      }
+      o = static_cast<int>(n == grid ? (o + t[k] % grid) % grid : (o + n) % grid);
+    }
+    return *std::max_element(load.begin(), load.end());
+  };
+  const double fine = deal(false, npieces, offset);
+  std::vector<int32_t> np_rows(nprob), off_rows(nprob);
+  const double rows = deal(true, np_rows.data(), off_rows.data());
+  if (rows < ROWS_MARGIN * fine)
+    for (int k = 0; k < nprob; ++k) {
+      npieces[k] = np_rows[k];
+      offset[k] = off_rows[k];
+    }
 }
 
 // ------------------------------------------------------------------ device state
@@ -493,7 +544,7 @@ int run(const serac_pair* pairs, int32_t n_pairs, const serac_params* params, co
 // bf16, the lists (slots x 4 quarters x K keys per row, slots = the most pieces that
 // cover one row tile).
 struct TopkPlan {
-  int K = 4, grid = 1, slots = 0, ldl = 0;
+  int K = 4, grid = 1, npieces = 1, slots = 0, ldl = 0;
   int64_t tiles = 0;
   size_t off_err = 0, off_staged = 0, off_lists = 0, total = 0;
   int64_t staged_rows = 0;
@@ -504,12 +555,13 @@ int topk_plan(int32_t n_a, int32_t n_b, int32_t k, int sms, TopkPlan& tp) {
   tp.K = k <= 4 ? MODE_TOPK4 : MODE_TOPK8;
   tp.tiles = problem_tiles(n_a, n_b);
   tp.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({static_cast<int64_t>(sms), tp.tiles, MAX_GRID})));
+  tp.npieces = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tp.grid, tp.tiles)));
   tp.ldl = static_cast<int>(round_up(std::max(n_a, 1), BM));
   tp.slots = 0;
   const int64_t ct = col_tiles(n_b);
   for (int64_t rt = 0; tp.tiles > 0 && rt < row_tiles(n_a); ++rt) {
     const int64_t t0 = rt * ct, t1 = std::min(tp.tiles, t0 + ct);
-    tp.slots = std::max(tp.slots, piece_of(t1 - 1, tp.tiles, tp.grid) - piece_of(t0, tp.tiles, tp.grid) + 1);
+    tp.slots = std::max(tp.slots, piece_of(t1 - 1, tp.tiles, tp.npieces) - piece_of(t0, tp.tiles, tp.npieces) + 1);
   }
   tp.staged_rows = round_up(n_a, PAD_ROWS) + round_up(n_b, PAD_ROWS);
   size_t off = 0;
@@ -570,7 +622,7 @@ int run_topk(const uint8_t* a, int32_t n_a, const uint8_t* b, int32_t n_b, int32
     f.b_row0 = b_row0;
     f.n_a = n_a;
     f.n_b = n_b;
-    f.npieces = static_cast<int32_t>(std::min<int64_t>(tp.grid, tp.tiles));
+    f.npieces = tp.npieces;
     f.offset = 0;
     f.ldl = tp.ldl;
     f.keys = lists;
@@ -589,7 +641,7 @@ int run_topk(const uint8_t* a, int32_t n_a, const uint8_t* b, int32_t n_b, int32
   mp.n_a = n_a;
   mp.n_b = n_b;
   mp.ldl = tp.ldl;
-  mp.grid = tp.grid;
+  mp.npieces = tp.npieces;
   mp.k = k;
   mp.scores = scores;
   mp.index = index;
@@ -767,7 +819,8 @@ int serac_schedule_describe(const serac_pair* pairs, int32_t n_pairs, int32_t gr
     for (int c = 0; c < grid; ++c) cta_tiles[c] = 0;
     for (int k = 0; k < nprob; ++k) {
       const int64_t t = chunk_problem_tiles(pairs, ch.p0, k);
-      for (int i = 0; i < npieces[k]; ++i) cta_tiles[(offset[k] + i) % g] += static_cast<int32_t>(piece_tiles(t, g, i));
+      for (int i = 0; i < npieces[k]; ++i)
+        cta_tiles[(offset[k] + i) % g] += static_cast<int32_t>(piece_tiles(t, npieces[k], i));
     }
   }
   return SERAC_OK;

@@ -94,8 +94,8 @@ struct Segment {
 };
 
 // Advances `cur` by one segment; false once the CTA has no work left.  Piece k of a
-// problem belongs to CTA (offset + k) mod grid: the problem's T tiles are dealt as
-// q = T / grid tiles per piece plus one more for the first r = T mod grid pieces, so
+// problem belongs to CTA (offset + k) mod grid: the problem's T tiles are dealt to its
+// n pieces as q = T / n tiles per piece plus one more for the first r = T mod n, so
 // piece k starts at tile k q + min(k, r).
 __device__ __forceinline__ bool next_segment(const FusedParams& P, Cursor& cur, Segment& g) {
   while (cur.t >= cur.tend) {
@@ -105,7 +105,7 @@ __device__ __forceinline__ bool next_segment(const FusedParams& P, Cursor& cur, 
     if (k < 0) k += P.grid;
     if (k >= fp.npieces) continue;
     const int tiles = ((fp.n_a + BM - 1) / BM) * ((fp.n_b + BN - 1) / BN);
-    const int q = tiles / P.grid, r = tiles - q * P.grid;
+    const int q = tiles / fp.npieces, r = tiles - q * fp.npieces;
     cur.k = k;
     cur.t = k * q + min(k, r);
     cur.tend = cur.t + q + (k < r ? 1 : 0);
@@ -239,7 +239,7 @@ __device__ __forceinline__ void topk_epilogue(const FusedParams& P, uint32_t tme
     if (ok && i < fp.n_a) {
       const int ct_total = (fp.n_b + BN - 1) / BN;
       const int64_t tiles = static_cast<int64_t>((fp.n_a + BM - 1) / BM) * ct_total;
-      const int slot = g.k - piece_of(static_cast<int64_t>(g.rt) * ct_total, tiles, P.grid);
+      const int slot = g.k - piece_of(static_cast<int64_t>(g.rt) * ct_total, tiles, fp.npieces);
 #pragma unroll
       for (int j = 0; j < K; ++j) fp.keys[topk_list_index(slot, qt, j, K, fp.ldl, i)] = R[j];
     }

@@ -11,10 +11,11 @@
 // single TMA tensor map covers; the zero rows score 0 and the zero floor drops them,
 // so ragged tails need no masking.
 //
-// Work: in a launch chunk, every CTA of the persistent fused kernel takes one piece
-// of every problem (piece k of problem p goes to CTA (offset_p + k) mod grid; a
-// problem's T tiles are dealt T / grid per piece, one more for the first T mod grid
-// pieces, and a problem with fewer tiles than CTAs has one-tile pieces).  A piece is a
+// Work: in a launch chunk, every problem's T tiles are cut into n <= grid pieces (T / n
+// tiles each, one more for the first T mod n); piece k of problem p goes to CTA
+// (offset_p + k) mod grid of the persistent fused kernel.  A single large pair is cut
+// into one piece per CTA; in a chunk with much more work than CTAs the pieces grow to
+// whole row tiles (see plan_pieces).  A piece is a
 // run of the problem's tiles in row-major order, processed as segments: one row tile
 // resident in shared memory against a run of column tiles, with one running top-2 per
 // row.  All CTAs thus work through the problems in the same order (a pair's two
@@ -62,10 +63,10 @@ constexpr int MODE_TOPK4 = 4;  // row top-4 per segment, written to segment list
 constexpr int MODE_TOPK8 = 8;  // row top-8 per segment, written to segment lists
 constexpr int MAX_TOPK = 8;
 
-// The piece that holds tile t when T tiles are dealt to `grid` CTAs (T / grid tiles
-// per piece and one more for the first T mod grid pieces).
-__host__ __device__ inline int32_t piece_of(int64_t t, int64_t T, int32_t grid) {
-  const int64_t q = T / grid, r = T % grid;
+// The piece that holds tile t when T tiles are dealt to n pieces (T / n tiles per piece
+// and one more for the first T mod n pieces).
+__host__ __device__ inline int32_t piece_of(int64_t t, int64_t T, int32_t n) {
+  const int64_t q = T / n, r = T % n;
   if (t < r * (q + 1)) return static_cast<int32_t>(t / (q + 1));
   return static_cast<int32_t>(r + (t - r * (q + 1)) / q);
 }
@@ -84,7 +85,7 @@ __host__ __device__ inline int64_t topk_list_index(int32_t slot, int32_t quarter
 
 struct TopkMergeParams {
   const unsigned long long* lists;
-  int32_t n_a, n_b, ldl, grid, k;  // k <= K: entries written per row
+  int32_t n_a, n_b, ldl, npieces, k;  // npieces: of the row problem; k <= K: entries written per row
   int32_t* scores;                 // [n_a][k]
   int32_t* index;                  // [n_a][k]
   int32_t* status;                 // SERAC_OK, or SERAC_ETIMEOUT when a kernel wait ran out (may be NULL)

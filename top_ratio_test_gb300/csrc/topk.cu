@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) topk_merge_kernel(const TopkMer
     const int rt = i / BM;
     const int64_t t0 = static_cast<int64_t>(rt) * ct_total;
     const int64_t t1 = t0 + ct_total < tiles ? t0 + ct_total : tiles;
-    const int slots = piece_of(t1 - 1, tiles, p.grid) - piece_of(t0, tiles, p.grid) + 1;
+    const int slots = piece_of(t1 - 1, tiles, p.npieces) - piece_of(t0, tiles, p.npieces) + 1;
     for (int slot = 0; slot < slots; ++slot) {
       unsigned long long y[K];
 #pragma unroll
