@@ -235,10 +235,12 @@ int match_pair_noalloc(const uint8_t* desc_a, int32_t n_a, const uint8_t* desc_b
  * CTAs (1..256), report the number of launch chunks and, for the first chunk, the
  * total number of pieces, the pieces of each problem (out_npieces[2 x pairs of that
  * chunk]: entry 2k for pair k's A rows, 2k + 1 for its B rows; a problem's tiles are
- * cut into that many runs, one per CTA, 0 for an empty problem) and the tiles each
- * CTA processes (cta_tiles[grid]; CTAs beyond the chunk's launch grid, which has at
- * most one CTA per tile, get 0).  Any output may be NULL.  Returns SERAC_EINVAL on
- * bad input. */
+ * cut into that many runs of consecutive tiles, each run on its own CTA, 0 for an
+ * empty problem -- one run per CTA for a single large pair, whole row tiles for a chunk
+ * of many equal pairs, whichever a cost model of the CTAs' loads and segment starts
+ * prefers) and the tiles each CTA processes (cta_tiles[grid]; CTAs beyond the chunk's
+ * launch grid, which has at most one CTA per tile, get 0).  Any output may be NULL.
+ * Returns SERAC_EINVAL on bad input. */
 int serac_schedule_describe(const serac_pair* pairs, int32_t n_pairs, int32_t grid, int32_t* out_chunks,
                             int32_t* out_pieces, int32_t* out_npieces, int32_t* cta_tiles);
 
